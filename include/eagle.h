@@ -1,0 +1,224 @@
+/*
+ * eagle.h — C ABI of the GB300 (sm_103a) implementation of one EAGLE-2
+ * tree-speculative decoding step.
+ *
+ * The step has four stages, each an entry point below:
+ *   eagle_draft_topk  per-row softmax statistics and top-k of the draft logits
+ *   eagle_tree_build  global scores, top-k frontier expansion, top-m rerank,
+ *                     node order (and, optionally, the attention mask)
+ *   eagle_tree_mask   ancestor-only attention mask from parent pointers
+ *   eagle_tree_attn   tree-masked attention of the tree nodes over the KV prefix
+ *   eagle_verify      greedy or speculative-sampling verification walk
+ *
+ * Sources (the pages the method is taken from):
+ *   [EAGLE-2] "論文解説: EAGLE-2 - 動的ドラフトツリーによるLLM推論の高速化"
+ *             (0h-n0.github.io, paper 2406.16858)
+ *   [EAGLE-1] abeam.tech explainer of "EAGLE: Speculative Sampling Requires
+ *             Rethinking Feature Uncertainty" (ICML 2024)
+ *
+ * Conventions for every entry point:
+ *   - All array pointers are DEVICE pointers owned by the caller; the library
+ *     never allocates, frees or keeps them.  Scratch memory is passed in as
+ *     `workspace` (size from the matching *_workspace_size query); it must be
+ *     zero-filled before its first use, and every call leaves it zeroed where
+ *     that matters (its split-merge counters), so it can be reused as is.
+ *     One workspace must not be used by two calls that may overlap on the GPU.
+ *   - Every call is asynchronous on `stream` (NULL = the legacy default
+ *     stream).  The return value reports argument and launch errors only:
+ *     EAGLE_OK, EAGLE_ERR_INVALID (bad argument, nothing launched),
+ *     EAGLE_ERR_UNSUPPORTED (valid but not implemented, nothing launched),
+ *     EAGLE_ERR_WORKSPACE (workspace too small), EAGLE_ERR_CUDA (a CUDA error
+ *     was reported while launching).
+ *   - Errors found on the device (inputs outside the documented domain) are
+ *     written to an optional device `status` word as a nonzero eagle_status;
+ *     the word is never written on success, so the caller zeroes it first.
+ *     No kernel traps or aborts.
+ *   - Layouts are dense row-major in the index order given, unless a leading
+ *     dimension `ld` (in elements) is given.  Pointers to 16-bit or 32-bit
+ *     logits and to attention tensors must be 16-byte aligned.
+ */
+#ifndef EAGLE_H
+#define EAGLE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *eagle_stream_t;
+
+typedef enum {
+  EAGLE_OK = 0,
+  EAGLE_ERR_INVALID = -1,
+  EAGLE_ERR_UNSUPPORTED = -2,
+  EAGLE_ERR_CUDA = -3,
+  EAGLE_ERR_WORKSPACE = -4,
+  EAGLE_ERR_TIMEOUT = -5
+} eagle_status;
+
+typedef enum { EAGLE_F32 = 0, EAGLE_BF16 = 1 } eagle_dtype;
+
+typedef enum { EAGLE_GREEDY = 0, EAGLE_SAMPLE = 1 } eagle_mode;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *eagle_status_string(int code);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int eagle_version(void);
+
+/* ------------------------------------------------------------------------
+ * Stage 1 — draft softmax statistics and top-k.
+ * [EAGLE-2] section "ドラフトモデルのキャリブレーション": a draft token's
+ * confidence is the probability the draft model assigns it; it approximates
+ * the token's acceptance rate.  For each USED row x of the draft logits:
+ *   M = max_t x_t,  Z = sum_t exp(x_t - M),
+ *   tok[0..k-1] = the k largest logits, in order (ties -> lower token id),
+ *   conf[r] = exp(x_tok[r] - M) / Z,  stats = (M, ln Z).
+ * Used rows: [b, 0, 0] (the root's distribution) and [b, d, j] for
+ * d = 1..D-1, j = 0..k-1 (the j-th expanded node of tree layer d).  Rows
+ * [b, 0, 1..k-1] are neither read nor written.
+ *
+ *   logits  device, dtype `dtype`, row [b, d, j] starts at element
+ *           ((b*D + d)*k + j) * ld; 16-byte aligned; V*elemsize and
+ *           ld*elemsize multiples of 16 bytes.  Values finite or -inf, at
+ *           least k finite per used row, no NaN.
+ *   tok     device int32 [B, D, k, k]     (out)
+ *   conf    device float [B, D, k, k]     (out)
+ *   stats   device float [B, D, k, 2]     (out; may be NULL)
+ * Limits: 1 <= k <= 32, k <= V, D >= 1, B >= 1.
+ * ------------------------------------------------------------------------ */
+size_t eagle_draft_topk_workspace_size(int B, int D, int k, int V);
+
+int eagle_draft_topk(const void *logits, int dtype, int B, int D, int k, int V,
+                     int64_t ld, int32_t *tok, float *conf, float *stats,
+                     void *workspace, size_t workspace_bytes,
+                     eagle_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Stage 2 — dynamic draft tree.
+ * [EAGLE-2] section "動的ドラフトツリーの構築アルゴリズム": V_i = product of
+ * the confidences on the root path (V_i equation); at every depth the k
+ * nodes with the largest V are expanded with their own top-k tokens; the m
+ * candidates with the largest V are kept; ancestors are added so the set is
+ * a connected tree.
+ * Computation (exactly): root = gid 0, V = 1.  Depth-1 candidates are the
+ * root row's tokens (gids 1..k).  For d = 1..D-1 the k depth-d candidates
+ * greatest in the key order (V desc, parent gid asc, token asc) are the
+ * expanded set E_d; E_d[j] takes row [d, j]; its children get
+ * V = fl32(V_parent * conf) (IEEE float multiply, round to nearest, no
+ * flush to zero) and gids numbered depth by depth, by j, then by child rank.
+ * The m candidates greatest in key order are kept.  With 0 <= conf <= 1 every
+ * ancestor precedes its descendants in key order, so the kept set is
+ * already connected (the ancestor step adds nothing).
+ * Output order: node 0 = root, nodes 1..m = kept candidates in key order, so
+ * parent index < node index.
+ *
+ *   tok, conf    device int32 / float [B, D, k, k], as written by stage 1
+ *                (tokens of one row distinct, 0 <= token < 2^20,
+ *                 0 <= conf <= 1)
+ *   root_tok     device int32 [B] or NULL (root token reported as -1)
+ *   node_tok     device int32 [B, m+1]  (out)
+ *   node_parent  device int32 [B, m+1]  (out; root -1)
+ *   node_depth   device int32 [B, m+1]  (out; may be NULL)
+ *   node_score   device float [B, m+1]  (out; V; may be NULL)
+ *   node_src     device int32 [B, m+1]  (out; candidate gid; may be NULL)
+ *   node_row     device int32 [B, m+1]  (out; d*k + j if the node was
+ *                expanded with row [d, j], root 0, else -1; may be NULL)
+ *   mask         device uint64 [B, m+1, W], W = ceil((m+1)/64) (out; may be
+ *                NULL) — the same words eagle_tree_mask writes
+ *   status       device int32 (out; may be NULL): EAGLE_ERR_INVALID when an
+ *                input is outside the domain above
+ * Limits: 1 <= k <= 32, D >= 1, 1 <= m <= k + (D-1)k^2 <= 4095.
+ * ------------------------------------------------------------------------ */
+int eagle_tree_build(const int32_t *tok, const float *conf, int B, int D, int k,
+                     int m, const int32_t *root_tok, int32_t *node_tok,
+                     int32_t *node_parent, int32_t *node_depth,
+                     float *node_score, int32_t *node_src, int32_t *node_row,
+                     uint64_t *mask, int32_t *status, eagle_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Ancestor-only attention mask.
+ * [EAGLE-2] section "注意マスクの調整": each token attends only to its
+ * ancestors.  Bit (j % 64) of word j / 64 of row i is set iff j == i or j is
+ * an ancestor of i (the root is an ancestor of every node).
+ *   node_parent  device int32 [B, n] (root -1, parent index < node index)
+ *   mask         device uint64 [B, n, ceil(n/64)] (out)
+ * Limits: 1 <= n <= 4096.
+ * ------------------------------------------------------------------------ */
+int eagle_tree_mask(const int32_t *node_parent, int B, int n, uint64_t *mask,
+                    eagle_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Stage 3 — tree attention.
+ * [EAGLE-1] sections "用語解説" (Tree Attention) and "Tree Attention の役割":
+ * the target scores every branch of the tree in one forward pass; with the
+ * [EAGLE-2] mask each tree node attends to the prefix and to its own
+ * ancestors.  For node i (0..n-1, n = m+1), query head h, KV head
+ * g = h / (Hq/Hkv):
+ *   keys = k_cache[b, g, 0:kv_len[b]]  ++  { k_tree[b, g, j] : mask bit j of row i }
+ *   s = scale * <q[b, i, h], key>,  out[b, i, h] = softmax(s) . values,
+ *   lse[b, i, h] = ln sum exp(s).
+ *   q          [B, n, Hq, dh]        dtype
+ *   k_cache    [B, Hkv, Lmax, dh]    dtype   (v_cache alike)
+ *   kv_len     device int32 [B], 0 <= kv_len[b] <= Lmax
+ *   k_tree     [B, Hkv, n, dh]       dtype   (v_tree alike)
+ *   mask       device uint64 [B, n, ceil(n/64)] (as eagle_tree_mask writes)
+ *   out        [B, n, Hq, dh]        dtype   (out)
+ *   lse        device float [B, n, Hq]  (out; may be NULL)
+ * Arithmetic: fp32 accumulation and softmax; bf16 inputs use the tensor
+ * cores.  Limits: Hq % Hkv == 0, dh in {64, 128}, 1 <= n <= 4096.
+ * ------------------------------------------------------------------------ */
+size_t eagle_tree_attn_workspace_size(int dtype, int B, int n, int Hq, int Hkv,
+                                      int dh, int Lmax);
+
+int eagle_tree_attn(const void *q, const void *k_cache, const void *v_cache,
+                    const int32_t *kv_len, const void *k_tree,
+                    const void *v_tree, const uint64_t *mask, int dtype, int B,
+                    int n, int Hq, int Hkv, int dh, int Lmax, float scale,
+                    void *out, float *lse, void *workspace,
+                    size_t workspace_bytes, eagle_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Stage 4 — verification walk.
+ * [EAGLE-1] section "検証方法": each draft token is accepted or rejected by
+ * the ratio of target and draft distributions; after a rejection the rest is
+ * discarded and a token resampled; the output follows the target exactly
+ * ([EAGLE-2]: lossless, rejection sampling as in EAGLE-1; temp=0 greedy).
+ * Row i of the target logits is the target's distribution after node i.
+ *   GREEDY: from the root, a = argmax of the current row (ties -> lower
+ *     token); move to the child carrying a while one exists; a is the bonus.
+ *   SAMPLE (temperature T > 0): children are point-mass drafts.  With
+ *     e_t = exp(x_t/T - max), Z = sum e, S = tokens rejected at this node:
+ *     child x (token t) is accepted iff u[b,x,0] * (Z - sum_S e) < e_t;
+ *     otherwise t joins S.  With no child accepted, the bonus is the
+ *     smallest t not in S whose cumulative residual mass exceeds
+ *     u[b,cur,1] * (Z - sum_S e).  Children are tried in node-index order.
+ *   target     dtype, row (b, i) starts at element (b*(m+1) + i) * ld
+ *   node_tok, node_parent   device int32 [B, m+1] (as stage 2 writes)
+ *   uniforms   device float [B, m+1, 2] in [0, 1) (SAMPLE; NULL for GREEDY)
+ *   accept_len device int32 [B]            (out; accepted draft tokens)
+ *   path_nodes device int32 [B, D+1]       (out; root first; -1 padded)
+ *   out_tokens device int32 [B, D+1]       (out; accepted tokens, then the
+ *                                           bonus token; -1 padded)
+ *   status     device int32 (out; may be NULL)
+ * D bounds the tree depth.  Limits: V*elemsize and ld*elemsize multiples of
+ * 16 bytes; 1 <= m+1 <= 4096; D >= 1.
+ * ------------------------------------------------------------------------ */
+size_t eagle_verify_workspace_size(int B, int m, int V);
+
+int eagle_verify(const void *target, int dtype, int64_t ld,
+                 const int32_t *node_tok, const int32_t *node_parent, int B,
+                 int m, int D, int V, int mode, float temperature,
+                 const float *uniforms, int32_t *accept_len,
+                 int32_t *path_nodes, int32_t *out_tokens, int32_t *status,
+                 void *workspace, size_t workspace_bytes,
+                 eagle_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EAGLE_H */

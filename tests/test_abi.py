@@ -1,0 +1,89 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library must load, export every function include/eagle.h declares, and
+reject invalid arguments before touching the device.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import tree_speculative_decoding_eagle_gb300 as eg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "eagle.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(eagle_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from tree_speculative_decoding_eagle_gb300 import build
+    build.build()
+    return eg.load_library()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(eg.EXPORTED)
+
+
+def test_status_strings(lib):
+    assert lib.eagle_status_string(0) == b"ok"
+    assert lib.eagle_status_string(-1) == b"invalid argument"
+    assert lib.eagle_status_string(-5) == b"device wait timed out"
+    assert lib.eagle_status_string(12345) == b"unknown status"
+    assert lib.eagle_version() >= 100
+
+
+NULL = None
+
+
+def test_invalid_arguments_are_rejected_on_the_host(lib):
+    fake = ctypes.c_void_p(0x1000)      # never dereferenced: validation fails first
+    unal = ctypes.c_void_p(0x1008)
+    # draft_topk: null logits, k > 32, k > V, misaligned V, misaligned pointer
+    assert lib.eagle_draft_topk(NULL, 1, 1, 2, 4, 64, 64, fake, fake, NULL, NULL, 0, NULL) == -1
+    assert lib.eagle_draft_topk(fake, 1, 1, 2, 33, 64, 64, fake, fake, NULL, NULL, 0, NULL) == -1
+    assert lib.eagle_draft_topk(fake, 1, 1, 2, 9, 8, 8, fake, fake, NULL, NULL, 0, NULL) == -1
+    assert lib.eagle_draft_topk(fake, 1, 1, 2, 4, 60, 60, fake, fake, NULL, NULL, 0, NULL) == -1
+    assert lib.eagle_draft_topk(unal, 1, 1, 2, 4, 64, 64, fake, fake, NULL, NULL, 0, NULL) == -1
+    assert lib.eagle_draft_topk(fake, 7, 1, 2, 4, 64, 64, fake, fake, NULL, NULL, 0, NULL) == -1
+    # tree_build: m larger than the candidate count, too many candidates
+    args = [fake, fake, 1, 2, 2, 7, NULL, fake, fake, NULL, NULL, NULL, NULL, NULL, NULL, NULL]
+    assert lib.eagle_tree_build(*args) == -1
+    args[3], args[4], args[5] = 6, 32, 10       # 32 + 5*1024 > 4095
+    assert lib.eagle_tree_build(*args) == -1
+    # tree_mask: n out of range
+    assert lib.eagle_tree_mask(fake, 1, 0, fake, NULL) == -1
+    assert lib.eagle_tree_mask(fake, 1, 5000, fake, NULL) == -1
+    # tree_attn: Hq not a multiple of Hkv, unsupported head dim
+    a = [fake] * 7 + [1, 1, 3, 6, 4, 64, 16, ctypes.c_float(0.1), fake, NULL, NULL, 0, NULL]
+    assert lib.eagle_tree_attn(*a) == -1
+    a[10], a[11], a[12] = 8, 4, 96
+    assert lib.eagle_tree_attn(*a) == -2
+    # verify: sampling without uniforms, non-positive temperature, bad mode
+    v = [fake, 1, 64, fake, fake, 1, 3, 2, 64, 1, ctypes.c_float(1.0), NULL, fake, fake, fake,
+         NULL, fake, 1 << 20, NULL]
+    assert lib.eagle_verify(*v) == -1
+    v[11] = fake
+    v[10] = ctypes.c_float(0.0)
+    assert lib.eagle_verify(*v) == -1
+    v[10] = ctypes.c_float(1.0)
+    v[9] = 5
+    assert lib.eagle_verify(*v) == -1
+
+
+def test_workspace_queries_are_host_only(lib):
+    assert lib.eagle_verify_workspace_size(8, 50, 32000) == 16 * 8 * 51 * 16
+    assert lib.eagle_draft_topk_workspace_size(1, 6, 10, 32000) > 0
+    assert lib.eagle_draft_topk_workspace_size(0, 6, 10, 32000) == 0

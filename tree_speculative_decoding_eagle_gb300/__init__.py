@@ -1,0 +1,217 @@
+"""Python binding of libeagle.so, the sm_103a implementation of one EAGLE-2
+tree-speculative decoding step.
+
+Each function below marshals torch CUDA tensors into the C ABI declared in
+include/eagle.h and calls it on the current CUDA stream; every step of the
+computation runs in the library's kernels.  There is no fallback: if the
+library is missing or a call reports an error, an exception is raised.
+
+    draft_topk  -> eagle_draft_topk   (softmax statistics + top-k per draft row)
+    tree_build  -> eagle_tree_build   (global scores, expansion, rerank, mask)
+    tree_mask   -> eagle_tree_mask    (ancestor-only attention mask)
+    tree_attn   -> eagle_tree_attn    (tree-masked attention over the KV prefix)
+    verify      -> eagle_verify       (greedy / speculative-sampling walk)
+"""
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libeagle.so")
+
+F32, BF16 = 0, 1
+GREEDY, SAMPLE = 0, 1
+
+EXPORTED = (
+    "eagle_status_string", "eagle_version",
+    "eagle_draft_topk_workspace_size", "eagle_draft_topk",
+    "eagle_tree_build", "eagle_tree_mask",
+    "eagle_tree_attn_workspace_size", "eagle_tree_attn",
+    "eagle_verify_workspace_size", "eagle_verify",
+)
+
+_lib = None
+
+
+class EagleError(RuntimeError):
+    pass
+
+
+def load_library(path=LIB_PATH):
+    """Load libeagle.so (built by tree_speculative_decoding_eagle_gb300.build)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise EagleError(f"{path} is missing: run `python -m tree_speculative_decoding_eagle_gb300.build`")
+    lib = ctypes.CDLL(path)
+    P, I, I64, SZ, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+    sig = {
+        "eagle_status_string": (ctypes.c_char_p, [I]),
+        "eagle_version": (I, []),
+        "eagle_draft_topk_workspace_size": (SZ, [I, I, I, I]),
+        "eagle_draft_topk": (I, [P, I, I, I, I, I, I64, P, P, P, P, SZ, P]),
+        "eagle_tree_build": (I, [P, P, I, I, I, I, P, P, P, P, P, P, P, P, P, P]),
+        "eagle_tree_mask": (I, [P, I, I, P, P]),
+        "eagle_tree_attn_workspace_size": (SZ, [I, I, I, I, I, I, I]),
+        "eagle_tree_attn": (I, [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, P, P, SZ, P]),
+        "eagle_verify_workspace_size": (SZ, [I, I, I]),
+        "eagle_verify": (I, [P, I, I64, P, P, I, I, I, I, I, F, P, P, P, P, P, P, SZ, P]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(t):
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise EagleError(f"unsupported dtype {t.dtype}")
+
+
+def _check(rc, what):
+    if rc != 0:
+        msg = load_library().eagle_status_string(rc).decode()
+        raise EagleError(f"{what} failed: {msg} ({rc})")
+
+
+def _cuda(t, name):
+    if not t.is_cuda:
+        raise EagleError(f"{name} must be a CUDA tensor")
+    return t
+
+
+class Workspace:
+    """Zero-initialised device scratch, grown on demand and reused."""
+
+    def __init__(self, device=None):
+        self.device = device
+        self.buf = None
+
+    def get(self, nbytes):
+        if nbytes == 0:
+            return None, 0
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.zeros(nbytes, dtype=torch.uint8, device=self.device or "cuda")
+        return self.buf, self.buf.numel()
+
+
+def draft_topk(logits, k, tok=None, conf=None, stats=None, workspace=None, stream=None):
+    """logits [B, D, k, V(ld)] -> tok int32 [B,D,k,k], conf f32, stats f32 [B,D,k,2]."""
+    lib = load_library()
+    _cuda(logits, "logits")
+    B, D, kk, V = logits.shape
+    if kk != k or logits.stride(-1) != 1:
+        raise EagleError("logits must be [B, D, k, V] with unit stride in V")
+    ld = logits.stride(2)
+    if logits.stride(1) != k * ld or logits.stride(0) != D * k * ld:
+        raise EagleError("logits rows must be evenly spaced")
+    dev = logits.device
+    tok = tok if tok is not None else torch.empty((B, D, k, k), dtype=torch.int32, device=dev)
+    conf = conf if conf is not None else torch.empty((B, D, k, k), dtype=torch.float32, device=dev)
+    stats = stats if stats is not None else torch.empty((B, D, k, 2), dtype=torch.float32, device=dev)
+    ws = workspace or Workspace(dev)
+    wbuf, wbytes = ws.get(lib.eagle_draft_topk_workspace_size(B, D, k, V))
+    _check(lib.eagle_draft_topk(_ptr(logits), _dtype_code(logits), B, D, k, V, ld, _ptr(tok),
+                                _ptr(conf), _ptr(stats), _ptr(wbuf), wbytes, _stream(stream)),
+           "eagle_draft_topk")
+    return tok, conf, stats
+
+
+def tree_build(tok, conf, m, root_tok=None, with_mask=True, out=None, status=None, stream=None):
+    """tok/conf [B, D, k, k] -> dict of node arrays [B, m+1] (+ mask [B, m+1, W])."""
+    lib = load_library()
+    _cuda(tok, "tok")
+    B, D, k, _ = tok.shape
+    n = m + 1
+    dev = tok.device
+    W = (n + 63) // 64
+    o = out or {}
+    o.setdefault("tok", torch.empty((B, n), dtype=torch.int32, device=dev))
+    o.setdefault("parent", torch.empty((B, n), dtype=torch.int32, device=dev))
+    o.setdefault("depth", torch.empty((B, n), dtype=torch.int32, device=dev))
+    o.setdefault("score", torch.empty((B, n), dtype=torch.float32, device=dev))
+    o.setdefault("src", torch.empty((B, n), dtype=torch.int32, device=dev))
+    o.setdefault("row", torch.empty((B, n), dtype=torch.int32, device=dev))
+    if with_mask:
+        o.setdefault("mask", torch.empty((B, n, W), dtype=torch.int64, device=dev))
+    _check(lib.eagle_tree_build(_ptr(tok), _ptr(conf), B, D, k, m, _ptr(root_tok), _ptr(o["tok"]),
+                                _ptr(o["parent"]), _ptr(o["depth"]), _ptr(o["score"]),
+                                _ptr(o["src"]), _ptr(o["row"]), _ptr(o.get("mask")),
+                                _ptr(status), _stream(stream)), "eagle_tree_build")
+    return o
+
+
+def tree_mask(node_parent, mask=None, stream=None):
+    """node_parent int32 [B, n] -> mask int64 (uint64 bit pattern) [B, n, W]."""
+    lib = load_library()
+    _cuda(node_parent, "node_parent")
+    B, n = node_parent.shape
+    W = (n + 63) // 64
+    mask = mask if mask is not None else torch.empty((B, n, W), dtype=torch.int64, device=node_parent.device)
+    _check(lib.eagle_tree_mask(_ptr(node_parent), B, n, _ptr(mask), _stream(stream)), "eagle_tree_mask")
+    return mask
+
+
+def tree_attn(q, k_cache, v_cache, kv_len, k_tree, v_tree, mask, scale=None, out=None,
+              lse=None, workspace=None, stream=None):
+    """q [B,n,Hq,dh], caches [B,Hkv,Lmax,dh], tree KV [B,Hkv,n,dh] -> out, lse."""
+    lib = load_library()
+    for t, nm in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (k_tree, "k_tree"),
+                  (v_tree, "v_tree"), (kv_len, "kv_len"), (mask, "mask")):
+        _cuda(t, nm)
+        if not t.is_contiguous():
+            raise EagleError(f"{nm} must be contiguous")
+    B, n, Hq, dh = q.shape
+    Hkv, Lmax = k_cache.shape[1], k_cache.shape[2]
+    dt = _dtype_code(q)
+    scale = dh ** -0.5 if scale is None else scale
+    out = out if out is not None else torch.empty_like(q)
+    lse = lse if lse is not None else torch.empty((B, n, Hq), dtype=torch.float32, device=q.device)
+    ws = workspace or Workspace(q.device)
+    wbuf, wbytes = ws.get(lib.eagle_tree_attn_workspace_size(dt, B, n, Hq, Hkv, dh, Lmax))
+    _check(lib.eagle_tree_attn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), _ptr(k_tree),
+                               _ptr(v_tree), _ptr(mask), dt, B, n, Hq, Hkv, dh, Lmax,
+                               ctypes.c_float(scale), _ptr(out), _ptr(lse), _ptr(wbuf), wbytes,
+                               _stream(stream)), "eagle_tree_attn")
+    return out, lse
+
+
+def verify(target, node_tok, node_parent, D, mode, temperature=1.0, uniforms=None,
+           accept_len=None, path_nodes=None, out_tokens=None, status=None, workspace=None,
+           stream=None):
+    """target [B, m+1, V] -> accept_len [B], path_nodes [B, D+1], out_tokens [B, D+1]."""
+    lib = load_library()
+    _cuda(target, "target")
+    B, n, V = target.shape
+    if target.stride(-1) != 1 or target.stride(0) != n * target.stride(1):
+        raise EagleError("target must be [B, m+1, V] with evenly spaced rows")
+    ld = target.stride(1)
+    m = n - 1
+    dev = target.device
+    accept_len = accept_len if accept_len is not None else torch.empty(B, dtype=torch.int32, device=dev)
+    path_nodes = path_nodes if path_nodes is not None else torch.empty((B, D + 1), dtype=torch.int32, device=dev)
+    out_tokens = out_tokens if out_tokens is not None else torch.empty((B, D + 1), dtype=torch.int32, device=dev)
+    ws = workspace or Workspace(dev)
+    wbuf, wbytes = ws.get(lib.eagle_verify_workspace_size(B, m, V))
+    mode_code = GREEDY if mode in ("greedy", GREEDY) else SAMPLE
+    _check(lib.eagle_verify(_ptr(target), _dtype_code(target), ld, _ptr(node_tok), _ptr(node_parent),
+                            B, m, D, V, mode_code, ctypes.c_float(temperature), _ptr(uniforms),
+                            _ptr(accept_len), _ptr(path_nodes), _ptr(out_tokens), _ptr(status),
+                            _ptr(wbuf), wbytes, _stream(stream)), "eagle_verify")
+    return accept_len, path_nodes, out_tokens

@@ -1,0 +1,165 @@
+// Device helpers shared by the kernels of the tree-speculative step.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/eagle.h"
+
+namespace eagle {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// ---- float <-> order-preserving unsigned ---------------------------------
+// Maps floats to uint32 so that unsigned comparison equals float comparison
+// (-0 is first folded into +0 so equal logits compare equal).
+__device__ __forceinline__ uint32_t ordered_u32(float x) {
+  x = x + 0.0f;  // -0 -> +0 under round-to-nearest
+  uint32_t u = __float_as_uint(x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float from_ordered_u32(uint32_t o) {
+  uint32_t u = (o & 0x80000000u) ? (o & 0x7fffffffu) : ~o;
+  return __uint_as_float(u);
+}
+
+// Top-k key of a logit: larger key = larger logit, then lower token id.
+__device__ __forceinline__ uint64_t topk_key(float x, uint32_t tok) {
+  return (static_cast<uint64_t>(ordered_u32(x)) << 32) | static_cast<uint64_t>(~tok);
+}
+__device__ __forceinline__ float key_value(uint64_t key) {
+  return from_ordered_u32(static_cast<uint32_t>(key >> 32));
+}
+__device__ __forceinline__ uint32_t key_token(uint64_t key) {
+  return ~static_cast<uint32_t>(key);
+}
+
+// ---- fast base-2 exponential (hardware approximation, PTX ex2.approx) ----
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ---- bf16 unpacking -------------------------------------------------------
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+template <typename T> struct VecTraits;
+template <> struct VecTraits<float> {
+  static constexpr int kElems = 4;  // per 16-byte vector
+  __device__ __forceinline__ static void unpack(const uint4 &v, float (&x)[4]) {
+    x[0] = __uint_as_float(v.x); x[1] = __uint_as_float(v.y);
+    x[2] = __uint_as_float(v.z); x[3] = __uint_as_float(v.w);
+  }
+  __device__ __forceinline__ static float load1(const void *p, int64_t i) {
+    return __ldg(reinterpret_cast<const float *>(p) + i);
+  }
+};
+template <> struct VecTraits<__nv_bfloat16> {
+  static constexpr int kElems = 8;
+  __device__ __forceinline__ static void unpack(const uint4 &v, float (&x)[8]) {
+    x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
+    x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z); x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
+  }
+  __device__ __forceinline__ static float load1(const void *p, int64_t i) {
+    const unsigned short *s = reinterpret_cast<const unsigned short *>(p);
+    return __uint_as_float(static_cast<uint32_t>(__ldg(s + i)) << 16);
+  }
+};
+
+// Streaming 16-byte load that does not allocate in L1.
+__device__ __forceinline__ uint4 ld_stream16(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+// ---- warp reductions ------------------------------------------------------
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int o) {
+  uint32_t lo = static_cast<uint32_t>(v), hi = static_cast<uint32_t>(v >> 32);
+  lo = __shfl_xor_sync(0xffffffffu, lo, o);
+  hi = __shfl_xor_sync(0xffffffffu, hi, o);
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+__device__ __forceinline__ uint64_t shfl_u64(uint64_t v, int src) {
+  uint32_t lo = static_cast<uint32_t>(v), hi = static_cast<uint32_t>(v >> 32);
+  lo = __shfl_sync(0xffffffffu, lo, src);
+  hi = __shfl_sync(0xffffffffu, hi, src);
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
+// Merge of two (max, sum-of-exp relative to max) pairs.
+__device__ __forceinline__ void lse_combine(float &m, float &s, float m2, float s2) {
+  float mn = fmaxf(m, m2);
+  if (mn == -INFINITY) return;  // both empty
+  s = s * ex2_approx((m - mn) * kLog2e) + s2 * ex2_approx((m2 - mn) * kLog2e);
+  m = mn;
+}
+
+// ---- sorted top-K lists of unique 64-bit keys (descending) ---------------
+// Insert `key` into a register list kept in descending order (keys unique).
+template <int K>
+__device__ __forceinline__ void list_insert(uint64_t (&list)[K], uint64_t key) {
+#pragma unroll
+  for (int j = 0; j < K; ++j) {
+    uint64_t a = list[j];
+    bool gt = key > a;
+    list[j] = gt ? key : a;
+    key = gt ? a : key;
+  }
+}
+
+// Bitonic merge: keep the K largest of two descending lists A (registers)
+// and B (partner lane's list via shuffles), result descending in A.
+template <int K>
+__device__ __forceinline__ void list_merge_xor(uint64_t (&a)[K], int lane_xor) {
+  uint64_t b[K];
+#pragma unroll
+  for (int j = 0; j < K; ++j) b[j] = shfl_xor_u64(a[j], lane_xor);
+  // a[j] vs b[K-1-j]: elementwise max gives the top K as a bitonic sequence
+#pragma unroll
+  for (int j = 0; j < K; ++j) {
+    uint64_t o = b[K - 1 - j];
+    a[j] = a[j] > o ? a[j] : o;
+  }
+  // bitonic sort descending
+#pragma unroll
+  for (int s = K / 2; s > 0; s >>= 1) {
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+      if ((j & s) == 0) {
+        uint64_t x = a[j], y = a[j + s];
+        a[j] = x > y ? x : y;
+        a[j + s] = x > y ? y : x;
+      }
+    }
+  }
+}
+
+// Warp-wide top-K: after this every lane holds the warp's K largest keys.
+template <int K>
+__device__ __forceinline__ void warp_topk(uint64_t (&a)[K]) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) list_merge_xor<K>(a, o);
+}
+
+// ---- device-side status reporting -----------------------------------------
+__device__ __forceinline__ void report(int32_t *status, int code) {
+  if (status) atomicCAS(reinterpret_cast<int *>(status), 0, code);
+}
+
+}  // namespace eagle

@@ -1,0 +1,276 @@
+// Stage 2: dynamic draft tree (global scores, top-k expansion, top-m
+// rerank, node order) and the ancestor-only attention mask.
+//
+// [EAGLE-2] section "動的ドラフトツリーの構築アルゴリズム": V_i is the product
+// of the confidences on the root path; at each depth the k nodes with the
+// largest V are expanded, each with its own top-k tokens; the m candidates
+// with the largest V are kept and, with their ancestors, form a connected
+// tree.  Section "注意マスクの調整": each node attends only to its ancestors.
+//
+// One CTA per sequence, everything in shared memory.  A candidate is a
+// 64-bit key  bits(V):32 | (4095 - parent gid):12 | (2^20 - 1 - token):20,
+// so unsigned order is the rank order (V desc, parent gid asc, token asc)
+// and keys are unique.  Ranks are obtained by counting larger keys (8 lanes
+// per item, shuffle-reduced).  The running top-m list is merged with each
+// new layer by rank arithmetic, so the whole candidate set is never sorted.
+#include "common.cuh"
+
+namespace eagle {
+
+constexpr int kTreeThreads = 256;
+constexpr int kMaxGid = 4095;
+
+__device__ __forceinline__ uint64_t tree_key(float v, int pgid, int tok) {
+  return (static_cast<uint64_t>(__float_as_uint(v)) << 32) |
+         (static_cast<uint64_t>(kMaxGid - pgid) << 20) |
+         static_cast<uint64_t>(0xFFFFF - tok);
+}
+__device__ __forceinline__ float tkey_score(uint64_t k) { return __uint_as_float(static_cast<uint32_t>(k >> 32)); }
+__device__ __forceinline__ int tkey_parent(uint64_t k) { return kMaxGid - static_cast<int>((k >> 20) & 0xFFF); }
+__device__ __forceinline__ int tkey_token(uint64_t k) { return 0xFFFFF - static_cast<int>(k & 0xFFFFF); }
+
+struct TreeArgs {
+  const int32_t *tok;
+  const float *conf;
+  int B, D, k, m, NC;
+  const int32_t *root_tok;
+  int32_t *node_tok, *node_parent, *node_depth, *node_src, *node_row;
+  float *node_score;
+  uint64_t *mask;
+  int32_t *status;
+};
+
+// Count, for each of n_items items, how many keys of `set` exceed the item's
+// key; 8 lanes per item.  Must be called by the whole block.
+__device__ __forceinline__ void count_greater(const uint64_t *item_keys, int n_items,
+                                              const uint64_t *set, int n_set, int *out) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nwarps = blockDim.x >> 5;
+  for (int base = warp * 4; base < n_items; base += nwarps * 4) {
+    const int it = base + (lane >> 3);
+    const int sub = lane & 7;
+    int cnt = 0;
+    if (it < n_items) {
+      const uint64_t me = item_keys[it];
+      for (int q = sub; q < n_set; q += 8) cnt += set[q] > me;
+    }
+    cnt += __shfl_xor_sync(0xffffffffu, cnt, 1);
+    cnt += __shfl_xor_sync(0xffffffffu, cnt, 2);
+    cnt += __shfl_xor_sync(0xffffffffu, cnt, 4);
+    if (it < n_items && sub == 0) out[it] = cnt;
+  }
+}
+
+__device__ __forceinline__ int depth_of_gid(int g, int k) {
+  if (g == 0) return 0;
+  if (g <= k) return 1;
+  return 2 + (g - 1 - k) / (k * k);
+}
+__device__ __forceinline__ int layer_base(int d, int k) {  // first gid of depth d >= 1
+  return d == 1 ? 1 : 1 + k + (d - 2) * k * k;
+}
+
+// Ancestor-or-self bits of node i, word w, walking parent pointers held in
+// shared memory (at most n steps even on malformed input).
+__device__ __forceinline__ uint64_t mask_word(const int *par, int n, int i, int w) {
+  uint64_t bits = 0;
+  int j = i;
+  for (int steps = 0; j >= 0 && j < n && steps <= n; ++steps) {
+    if ((j >> 6) == w) bits |= 1ull << (j & 63);
+    j = par[j];
+  }
+  return bits;
+}
+
+__global__ void __launch_bounds__(kTreeThreads) tree_build_kernel(TreeArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int k = a.k, m = a.m, NC = a.NC, D = a.D;
+  const int kk = k * k;
+  const int n = m + 1;
+
+  // shared layout
+  uint64_t *s_key = reinterpret_cast<uint64_t *>(smem);        // [NC+1]
+  uint64_t *s_L = s_key + (NC + 1);                              // [2][m] keys
+  int *s_Lg = reinterpret_cast<int *>(s_L + 2 * m);              // [2][m] gids
+  int *s_cnt = s_Lg + 2 * m;                                     // [2*kk + m]
+  int *s_row = s_cnt + (2 * kk + m);                             // [NC+1]
+  int *s_out = s_row + (NC + 1);                                 // [NC+1] gid -> node
+  int *s_par = s_out + (NC + 1);                                 // [n]
+  int *s_E = s_par + n;                                          // [k]
+  __shared__ int s_bad;
+
+  const int32_t *tok = a.tok + static_cast<int64_t>(b) * D * kk;
+  const float *conf = a.conf + static_cast<int64_t>(b) * D * kk;
+
+  if (tid == 0) s_bad = 0;
+  for (int g = tid; g <= NC; g += blockDim.x) {
+    s_row[g] = -1;
+    s_out[g] = -1;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    s_row[0] = 0;
+    s_out[0] = 0;
+  }
+
+  // depth-1 layer: the root row's tokens
+  for (int r = tid; r < k; r += blockDim.x) {
+    int t = tok[r];
+    float c = conf[r];
+    if (!(c >= 0.f && c <= 1.f) || t < 0 || t > 0xFFFFF) s_bad = 1;
+    if (t < 0 || t > 0xFFFFF) t = 0;  // keep the key's fields in range
+    c = __fadd_rn(__fmul_rn(1.0f, c), 0.0f);
+    s_key[1 + r] = tree_key(c, 0, t);
+  }
+  int nL = 0, cur = 0;
+  for (int d = 1; d <= D; ++d) {
+    __syncthreads();
+    const int base = layer_base(d, k);
+    const int nl = d == 1 ? k : kk;
+    const uint64_t *layer = s_key + base;
+    uint64_t *L = s_L + cur * m;
+    int *Lg = s_Lg + cur * m;
+    // ranks within the layer, layer vs list, list vs layer
+    count_greater(layer, nl, layer, nl, s_cnt);
+    count_greater(layer, nl, L, nL, s_cnt + kk);
+    count_greater(L, nL, layer, nl, s_cnt + 2 * kk);
+    __syncthreads();
+    uint64_t *L2 = s_L + (cur ^ 1) * m;
+    int *Lg2 = s_Lg + (cur ^ 1) * m;
+    for (int q = tid; q < nl; q += blockDim.x) {
+      const int rank = s_cnt[q];
+      if (d < D && rank < k) {
+        s_E[rank] = base + q;
+        s_row[base + q] = d * k + rank;
+      }
+      const int pos = rank + s_cnt[kk + q];
+      if (pos < m) {
+        L2[pos] = layer[q];
+        Lg2[pos] = base + q;
+      }
+    }
+    for (int q = tid; q < nL; q += blockDim.x) {
+      const int pos = q + s_cnt[2 * kk + q];
+      if (pos < m) {
+        L2[pos] = L[q];
+        Lg2[pos] = Lg[q];
+      }
+    }
+    nL = min(m, nL + nl);
+    cur ^= 1;
+    if (d == D) break;
+    __syncthreads();
+    // children of the expanded nodes: row [d, j] for E[j]
+    const int nbase = layer_base(d + 1, k);
+    for (int q = tid; q < kk; q += blockDim.x) {
+      const int j = q / k, r = q % k;
+      const int p = s_E[j];
+      int t = tok[(d * k + j) * k + r];
+      const float c = conf[(d * k + j) * k + r];
+      if (!(c >= 0.f && c <= 1.f) || t < 0 || t > 0xFFFFF) s_bad = 1;
+      if (t < 0 || t > 0xFFFFF) t = 0;
+      const float v = __fadd_rn(__fmul_rn(tkey_score(s_key[p]), c), 0.0f);
+      s_key[nbase + q] = tree_key(v, p, t);
+    }
+  }
+  __syncthreads();
+
+  // ---- outputs ---------------------------------------------------------
+  const uint64_t *L = s_L + cur * m;
+  const int *Lg = s_Lg + cur * m;
+  for (int q = tid; q < m; q += blockDim.x) s_out[Lg[q]] = q + 1;
+  __syncthreads();
+  const int64_t ob = static_cast<int64_t>(b) * n;
+  for (int i = tid; i < n; i += blockDim.x) {
+    int t, par, dep, src, row;
+    float sc;
+    if (i == 0) {
+      t = a.root_tok ? a.root_tok[b] : -1;
+      par = -1; dep = 0; src = 0; row = 0; sc = 1.0f;
+    } else {
+      const uint64_t key = L[i - 1];
+      src = Lg[i - 1];
+      t = tkey_token(key);
+      sc = tkey_score(key);
+      par = s_out[tkey_parent(key)];
+      if (par < 0 || par >= i) s_bad = 1;  // not closed: a confidence outside [0, 1]
+      dep = depth_of_gid(src, k);
+      row = s_row[src];
+    }
+    s_par[i] = par;
+    a.node_tok[ob + i] = t;
+    a.node_parent[ob + i] = par;
+    if (a.node_depth) a.node_depth[ob + i] = dep;
+    if (a.node_score) a.node_score[ob + i] = sc;
+    if (a.node_src) a.node_src[ob + i] = src;
+    if (a.node_row) a.node_row[ob + i] = row;
+  }
+  __syncthreads();
+  if (a.mask) {
+    const int W = (n + 63) >> 6;
+    for (int q = tid; q < n * W; q += blockDim.x) {
+      const int i = q / W, w = q % W;
+      a.mask[(ob + i) * W + w] = mask_word(s_par, n, i, w);
+    }
+  }
+  if (tid == 0 && s_bad) report(a.status, EAGLE_ERR_INVALID);
+}
+
+__global__ void __launch_bounds__(256) tree_mask_kernel(const int32_t *parent, int n, uint64_t *mask) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  int *s_par = reinterpret_cast<int *>(smem);
+  const int b = blockIdx.x;
+  const int64_t ob = static_cast<int64_t>(b) * n;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) s_par[i] = parent[ob + i];
+  __syncthreads();
+  const int W = (n + 63) >> 6;
+  for (int q = threadIdx.x; q < n * W; q += blockDim.x) {
+    const int i = q / W, w = q % W;
+    mask[(ob + i) * W + w] = mask_word(s_par, n, i, w);
+  }
+}
+
+// ---- host side ---------------------------------------------------------------
+
+size_t tree_smem_bytes(int D, int k, int m) {
+  const int NC = k + (D - 1) * k * k;
+  const int kk = k * k, n = m + 1;
+  size_t bytes = sizeof(uint64_t) * (NC + 1)          // s_key
+               + sizeof(uint64_t) * 2 * m             // s_L
+               + sizeof(int) * 2 * m                  // s_Lg
+               + sizeof(int) * (2 * kk + m)           // s_cnt
+               + sizeof(int) * 2 * (NC + 1)           // s_row, s_out
+               + sizeof(int) * n + sizeof(int) * k;   // s_par, s_E
+  return (bytes + 15) / 16 * 16;
+}
+
+cudaError_t launch_tree_build(const int32_t *tok, const float *conf, int B, int D, int k, int m,
+                              const int32_t *root_tok, int32_t *node_tok, int32_t *node_parent,
+                              int32_t *node_depth, float *node_score, int32_t *node_src,
+                              int32_t *node_row, uint64_t *mask, int32_t *status, cudaStream_t st) {
+  TreeArgs a;
+  a.tok = tok; a.conf = conf;
+  a.B = B; a.D = D; a.k = k; a.m = m;
+  a.NC = k + (D - 1) * k * k;
+  a.root_tok = root_tok;
+  a.node_tok = node_tok; a.node_parent = node_parent; a.node_depth = node_depth;
+  a.node_src = node_src; a.node_row = node_row; a.node_score = node_score;
+  a.mask = mask; a.status = status;
+  const size_t smem = tree_smem_bytes(D, k, m);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(tree_build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  tree_build_kernel<<<B, kTreeThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tree_mask(const int32_t *parent, int B, int n, uint64_t *mask, cudaStream_t st) {
+  tree_mask_kernel<<<B, 256, sizeof(int) * n, st>>>(parent, n, mask);
+  return cudaGetLastError();
+}
+
+}  // namespace eagle

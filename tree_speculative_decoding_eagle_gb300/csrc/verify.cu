@@ -1,0 +1,358 @@
+// Stage 4: the verification walk over the draft tree.
+//
+// [EAGLE-1] section "検証方法": every draft token is accepted or rejected by
+// the ratio of target and draft distributions; after a rejection the rest of
+// the branch is discarded and a token is resampled, so the output follows
+// the target model exactly ([EAGLE-2]: lossless; temp=0 is greedy).
+// Children are point-mass drafts, so child x (token t) is accepted with
+// probability equal to t's residual target probability:
+//   accept iff u[x,0] * (Z - sum_{s in S} e_s) < e_t,
+// and the bonus token is drawn from the residual by inverse CDF with u[cur,1].
+//
+// Two kernels:
+//  (a) verify_stats: one pass over all target rows in HBM.  Each warp owns a
+//      2048-token chunk of a row and records (max, sum exp(y - max), argmax)
+//      of y = x / T; these do not depend on the tree, so the pass can run
+//      beside the draft stages.
+//  (b) verify_walk: one warp per sequence walks the tree using the chunk
+//      statistics, a handful of single-logit reads for the children's tokens
+//      and, for a bonus draw, one re-read of a single chunk.
+#include "common.cuh"
+
+namespace eagle {
+
+constexpr int kChunk = 2048;  // tokens per statistics chunk (64 per lane)
+
+struct alignas(16) ChunkStat {
+  float m;  // max of y over the chunk
+  float s;  // sum of exp(y - m) over the chunk (sampling mode)
+  int a;    // lowest token attaining m (greedy mode)
+  int pad;
+};
+
+struct VerifyArgs {
+  const void *target;
+  int64_t ld;
+  const int32_t *node_tok, *node_parent;
+  int B, m, n, D, V, nch, mode;
+  float inv_t;
+  const float *u;
+  int32_t *accept_len, *path_nodes, *out_tokens, *status;
+  ChunkStat *stats;
+};
+
+template <typename T, bool SAMPLE>
+__global__ void __launch_bounds__(256) verify_stats_kernel(VerifyArgs a) {
+  using VT = VecTraits<T>;
+  constexpr int VEC = VT::kElems;
+  constexpr int NVL = kChunk / VEC / 32;  // vectors per lane
+  const int lane = threadIdx.x & 31;
+  const int64_t total = static_cast<int64_t>(a.B) * a.n * a.nch;
+  const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t task = wid; task < total; task += nwarps) {
+    const int64_t row = task / a.nch;
+    const int c = static_cast<int>(task % a.nch);
+    const T *p = reinterpret_cast<const T *>(a.target) + row * a.ld;
+    const int t_begin = c * kChunk;
+    const int nvec = (min(a.V, t_begin + kChunk) - t_begin) / VEC;
+    uint4 buf[NVL];
+#pragma unroll
+    for (int i = 0; i < NVL; ++i) {
+      const int v = lane + 32 * i;
+      if (v < nvec) buf[i] = ld_stream16(p + t_begin + v * VEC);
+    }
+    float best = -INFINITY;
+    int arg = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < NVL; ++i) {
+      const int v = lane + 32 * i;
+      if (v < nvec) {
+        float x[VEC];
+        VT::unpack(buf[i], x);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          const float y = SAMPLE ? x[e] * a.inv_t : x[e];
+          if (y > best) {  // strict: first occurrence within the lane
+            best = y;
+            arg = t_begin + v * VEC + e;
+          }
+        }
+      }
+    }
+    const uint32_t om = __reduce_max_sync(0xffffffffu, ordered_u32(best));
+    const float M = from_ordered_u32(om);
+    ChunkStat st;
+    st.m = M;
+    st.pad = 0;
+    if (SAMPLE) {
+      float s = 0.f;
+      if (M > -INFINITY) {
+        const float mL = M * kLog2e;
+#pragma unroll
+        for (int i = 0; i < NVL; ++i) {
+          const int v = lane + 32 * i;
+          if (v < nvec) {
+            float x[VEC];
+            VT::unpack(buf[i], x);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) s += ex2_approx(fmaf(x[e] * a.inv_t, kLog2e, -mL));
+          }
+        }
+      }
+      st.s = warp_sum(s);
+      st.a = -1;
+    } else {
+      const uint32_t cand = (ordered_u32(best) == om) ? static_cast<uint32_t>(arg) : 0xffffffffu;
+      st.a = static_cast<int>(__reduce_min_sync(0xffffffffu, cand));
+      st.s = 0.f;
+    }
+    if (lane == 0) a.stats[task] = st;
+  }
+}
+
+// logit of token t in row `row`, scaled by 1/T
+template <typename T>
+__device__ __forceinline__ float logit_at(const VerifyArgs &a, int64_t row, int t) {
+  return VecTraits<T>::load1(a.target, row * a.ld + t);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(32) verify_walk_kernel(VerifyArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  int *s_par = reinterpret_cast<int *>(smem);
+  int *s_tok = s_par + a.n;
+  int *s_rej = s_tok + a.n;  // rejected tokens at the current node
+  const int b = blockIdx.x;
+  const int lane = threadIdx.x;
+  const int n = a.n;
+  const int64_t nb = static_cast<int64_t>(b) * n;
+  for (int i = lane; i < n; i += 32) {
+    s_par[i] = a.node_parent[nb + i];
+    s_tok[i] = a.node_tok[nb + i];
+  }
+  __syncwarp();
+  const bool sample = a.mode == EAGLE_SAMPLE;
+  int cur = 0, acc = 0, bonus = -1;
+  if (lane == 0) a.path_nodes[static_cast<int64_t>(b) * (a.D + 1)] = 0;
+
+  for (;;) {
+    const int64_t row = nb + cur;
+    const ChunkStat *cs = a.stats + row * a.nch;
+    // row maximum (and, greedy, the argmax) from the chunk statistics
+    float bm = -INFINITY;
+    int ba = 0x7fffffff;
+    for (int c = lane; c < a.nch; c += 32) {
+      const ChunkStat st = cs[c];
+      if (st.m > bm) { bm = st.m; ba = st.a; }  // chunks ascend in token order
+    }
+    const uint32_t om = __reduce_max_sync(0xffffffffu, ordered_u32(bm));
+    const float M = from_ordered_u32(om);
+    const float mL = M * kLog2e;
+    int next = -1;
+    float Z = 0.f, rej_sum = 0.f;
+    int n_rej = 0;
+    if (!sample) {
+      bonus = static_cast<int>(__reduce_min_sync(
+          0xffffffffu, ordered_u32(bm) == om ? static_cast<uint32_t>(ba) : 0xffffffffu));
+      for (int base = 0; base < n && next < 0; base += 32) {
+        const int i = base + lane;
+        const bool hit = i < n && s_par[i] == cur && s_tok[i] == bonus;
+        const unsigned bal = __ballot_sync(0xffffffffu, hit);
+        if (bal) next = base + __ffs(bal) - 1;
+      }
+    } else {
+      float z = 0.f;
+      for (int c = lane; c < a.nch; c += 32) {
+        const ChunkStat st = cs[c];
+        if (st.m > -INFINITY) z += st.s * ex2_approx(fmaf(st.m, kLog2e, -mL));
+      }
+      Z = warp_sum(z);
+      for (int base = 0; base < n && next < 0; base += 32) {
+        const int i = base + lane;
+        unsigned bal = __ballot_sync(0xffffffffu, i < n && s_par[i] == cur);
+        while (bal && next < 0) {
+          const int x = base + __ffs(bal) - 1;
+          bal &= bal - 1;
+          const int t = s_tok[x];
+          const bool t_ok = t >= 0 && t < a.V;
+          if (!t_ok && lane == 0) report(a.status, EAGLE_ERR_INVALID);
+          const float e = t_ok ? ex2_approx(fmaf(logit_at<T>(a, row, t) * a.inv_t, kLog2e, -mL)) : 0.f;
+          const float u0 = a.u[(nb + x) * 2 + 0];
+          if (u0 * (Z - rej_sum) < e) {
+            next = x;
+          } else {
+            rej_sum += e;
+            if (lane == 0) s_rej[n_rej] = t;
+            ++n_rej;
+          }
+        }
+      }
+      __syncwarp();
+    }
+    if (next < 0 || acc >= a.D) {
+      if (sample) {
+        // ---- bonus: inverse CDF of the residual over the row -------------
+        const float target = a.u[(nb + cur) * 2 + 1] * (Z - rej_sum);
+        // chunk masses; lane l owns a contiguous block of chunks
+        const int cpl = (a.nch + 31) / 32;
+        const int c0 = lane * cpl, c1 = min(a.nch, c0 + cpl);
+        double lane_mass = 0.0;
+        for (int c = c0; c < c1; ++c) {
+          const ChunkStat st = cs[c];
+          float w = st.m > -INFINITY ? st.s * ex2_approx(fmaf(st.m, kLog2e, -mL)) : 0.f;
+          for (int q = 0; q < n_rej; ++q) {
+            const int t = s_rej[q];
+            if (t >= 0 && t / kChunk == c) w -= ex2_approx(fmaf(logit_at<T>(a, row, t) * a.inv_t, kLog2e, -mL));
+          }
+          lane_mass += fmaxf(w, 0.f);
+        }
+        double incl = lane_mass;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const double v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        const double excl = incl - lane_mass;
+        const double tgt = static_cast<double>(target);
+        // first lane whose inclusive prefix exceeds the target (else the last lane with mass)
+        unsigned hitb = __ballot_sync(0xffffffffu, incl > tgt && lane_mass > 0.0);
+        unsigned nz = __ballot_sync(0xffffffffu, lane_mass > 0.0);
+        const int hl = hitb ? __ffs(hitb) - 1 : (nz ? 31 - __clz(nz) : 0);
+        // the owning lane finds the chunk
+        int chunk = -1;
+        double before = 0.0;
+        if (lane == hl) {
+          double run = excl;
+          int lastnz = -1;
+          double lastbefore = excl;
+          for (int c = c0; c < c1; ++c) {
+            const ChunkStat st = cs[c];
+            float w = st.m > -INFINITY ? st.s * ex2_approx(fmaf(st.m, kLog2e, -mL)) : 0.f;
+            for (int q = 0; q < n_rej; ++q) {
+              const int t = s_rej[q];
+              if (t >= 0 && t / kChunk == c) w -= ex2_approx(fmaf(logit_at<T>(a, row, t) * a.inv_t, kLog2e, -mL));
+            }
+            w = fmaxf(w, 0.f);
+            if (w > 0.f) { lastnz = c; lastbefore = run; }
+            if (run + w > tgt && w > 0.f) { chunk = c; before = run; break; }
+            run += w;
+          }
+          if (chunk < 0) { chunk = lastnz; before = lastbefore; }
+        }
+        chunk = __shfl_sync(0xffffffffu, chunk, hl);
+        before = __shfl_sync(0xffffffffu, before, hl);
+        if (chunk < 0) {  // no residual mass anywhere: inputs outside the domain
+          bonus = -1;
+          break;
+        }
+        // scan the chunk: lane l owns 64 consecutive tokens
+        const int tb = chunk * kChunk + lane * 64;
+        const int te = min(a.V, tb + 64);
+        float lane_w = 0.f;
+        for (int t = tb; t < te; ++t) {
+          bool in_s = false;
+          for (int q = 0; q < n_rej; ++q) in_s |= (s_rej[q] == t);
+          if (!in_s) lane_w += ex2_approx(fmaf(logit_at<T>(a, row, t) * a.inv_t, kLog2e, -mL));
+        }
+        double lincl = lane_w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const double v = __shfl_up_sync(0xffffffffu, lincl, o);
+          if (lane >= o) lincl += v;
+        }
+        const double lexcl = before + (lincl - lane_w);
+        lincl += before;
+        hitb = __ballot_sync(0xffffffffu, lincl > tgt && lane_w > 0.f);
+        nz = __ballot_sync(0xffffffffu, lane_w > 0.f);
+        const int hl2 = hitb ? __ffs(hitb) - 1 : (nz ? 31 - __clz(nz) : 0);
+        int tok = -1;
+        if (lane == hl2) {
+          double run = lexcl;
+          int lastnz = -1;
+          for (int t = tb; t < te; ++t) {
+            bool in_s = false;
+            for (int q = 0; q < n_rej; ++q) in_s |= (s_rej[q] == t);
+            if (in_s) continue;
+            const float w = ex2_approx(fmaf(logit_at<T>(a, row, t) * a.inv_t, kLog2e, -mL));
+            if (w > 0.f) lastnz = t;
+            run += w;
+            if (run > tgt && w > 0.f) { tok = t; break; }
+          }
+          if (tok < 0) tok = lastnz;
+        }
+        bonus = __shfl_sync(0xffffffffu, tok, hl2);
+      }
+      break;
+    }
+    cur = next;
+    ++acc;
+    if (lane == 0) {
+      a.path_nodes[static_cast<int64_t>(b) * (a.D + 1) + acc] = cur;
+      a.out_tokens[static_cast<int64_t>(b) * (a.D + 1) + acc - 1] = s_tok[cur];
+    }
+  }
+  if (lane == 0) {
+    const int64_t ob = static_cast<int64_t>(b) * (a.D + 1);
+    a.accept_len[b] = acc;
+    a.out_tokens[ob + acc] = bonus;
+    for (int q = acc + 1; q <= a.D; ++q) {
+      a.path_nodes[ob + q] = -1;
+      a.out_tokens[ob + q] = -1;
+    }
+    if (bonus < 0) report(a.status, EAGLE_ERR_INVALID);
+  }
+}
+
+// ---- host side ---------------------------------------------------------------
+
+int verify_chunks(int V) { return (V + kChunk - 1) / kChunk; }
+
+size_t verify_workspace_bytes(int B, int m, int V) {
+  return sizeof(ChunkStat) * static_cast<size_t>(B) * (m + 1) * verify_chunks(V);
+}
+
+template <typename T>
+static cudaError_t launch_verify_t(const VerifyArgs &a, int num_sms, cudaStream_t st) {
+  const int64_t tasks = static_cast<int64_t>(a.B) * a.n * a.nch;
+  int64_t blocks = (tasks + 7) / 8;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  if (a.mode == EAGLE_SAMPLE)
+    verify_stats_kernel<T, true><<<static_cast<int>(blocks), 256, 0, st>>>(a);
+  else
+    verify_stats_kernel<T, false><<<static_cast<int>(blocks), 256, 0, st>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const size_t smem = sizeof(int) * 3 * static_cast<size_t>(a.n);
+  if (smem > 48 * 1024) {
+    e = cudaFuncSetAttribute(verify_walk_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  verify_walk_kernel<T><<<a.B, 32, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_verify(const void *target, int dtype, int64_t ld, const int32_t *node_tok,
+                          const int32_t *node_parent, int B, int m, int D, int V, int mode,
+                          float temperature, const float *u, int32_t *accept_len,
+                          int32_t *path_nodes, int32_t *out_tokens, int32_t *status, void *ws,
+                          int num_sms, cudaStream_t st) {
+  VerifyArgs a;
+  a.target = target; a.ld = ld;
+  a.node_tok = node_tok; a.node_parent = node_parent;
+  a.B = B; a.m = m; a.n = m + 1; a.D = D; a.V = V;
+  a.nch = verify_chunks(V);
+  a.mode = mode;
+  a.inv_t = mode == EAGLE_SAMPLE ? 1.0f / temperature : 1.0f;
+  a.u = u;
+  a.accept_len = accept_len; a.path_nodes = path_nodes; a.out_tokens = out_tokens;
+  a.status = status;
+  a.stats = reinterpret_cast<ChunkStat *>(ws);
+  return dtype == EAGLE_BF16 ? launch_verify_t<__nv_bfloat16>(a, num_sms, st)
+                             : launch_verify_t<float>(a, num_sms, st);
+}
+
+}  // namespace eagle
