@@ -88,13 +88,16 @@ int eagle_version(void);
  *   tok     device int32 [B, D, k, k]     (out)
  *   conf    device float [B, D, k, k]     (out)
  *   stats   device float [B, D, k, 2]     (out; may be NULL)
+ *   status  device int32 (out; may be NULL): EAGLE_ERR_TIMEOUT if a bounded
+ *           wait on the kernel's own copies gave up (the row is then not
+ *           written)
  * Limits: 1 <= k <= 32, k <= V, D >= 1, B >= 1.
  * ------------------------------------------------------------------------ */
 size_t eagle_draft_topk_workspace_size(int B, int D, int k, int V);
 
 int eagle_draft_topk(const void *logits, int dtype, int B, int D, int k, int V,
                      int64_t ld, int32_t *tok, float *conf, float *stats,
-                     void *workspace, size_t workspace_bytes,
+                     int32_t *status, void *workspace, size_t workspace_bytes,
                      eagle_stream_t stream);
 
 /* ------------------------------------------------------------------------

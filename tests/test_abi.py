@@ -52,12 +52,12 @@ def test_invalid_arguments_are_rejected_on_the_host(lib):
     fake = ctypes.c_void_p(0x1000)      # never dereferenced: validation fails first
     unal = ctypes.c_void_p(0x1008)
     # draft_topk: null logits, k > 32, k > V, misaligned V, misaligned pointer
-    assert lib.eagle_draft_topk(NULL, 1, 1, 2, 4, 64, 64, fake, fake, NULL, NULL, 0, NULL) == -1
-    assert lib.eagle_draft_topk(fake, 1, 1, 2, 33, 64, 64, fake, fake, NULL, NULL, 0, NULL) == -1
-    assert lib.eagle_draft_topk(fake, 1, 1, 2, 9, 8, 8, fake, fake, NULL, NULL, 0, NULL) == -1
-    assert lib.eagle_draft_topk(fake, 1, 1, 2, 4, 60, 60, fake, fake, NULL, NULL, 0, NULL) == -1
-    assert lib.eagle_draft_topk(unal, 1, 1, 2, 4, 64, 64, fake, fake, NULL, NULL, 0, NULL) == -1
-    assert lib.eagle_draft_topk(fake, 7, 1, 2, 4, 64, 64, fake, fake, NULL, NULL, 0, NULL) == -1
+    assert lib.eagle_draft_topk(NULL, 1, 1, 2, 4, 64, 64, fake, fake, NULL, NULL, NULL, 0, NULL) == -1
+    assert lib.eagle_draft_topk(fake, 1, 1, 2, 33, 64, 64, fake, fake, NULL, NULL, NULL, 0, NULL) == -1
+    assert lib.eagle_draft_topk(fake, 1, 1, 2, 9, 8, 8, fake, fake, NULL, NULL, NULL, 0, NULL) == -1
+    assert lib.eagle_draft_topk(fake, 1, 1, 2, 4, 60, 60, fake, fake, NULL, NULL, NULL, 0, NULL) == -1
+    assert lib.eagle_draft_topk(unal, 1, 1, 2, 4, 64, 64, fake, fake, NULL, NULL, NULL, 0, NULL) == -1
+    assert lib.eagle_draft_topk(fake, 7, 1, 2, 4, 64, 64, fake, fake, NULL, NULL, NULL, 0, NULL) == -1
     # tree_build: m larger than the candidate count, too many candidates
     args = [fake, fake, 1, 2, 2, 7, NULL, fake, fake, NULL, NULL, NULL, NULL, NULL, NULL, NULL]
     assert lib.eagle_tree_build(*args) == -1

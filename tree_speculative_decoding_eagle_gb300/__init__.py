@@ -51,7 +51,7 @@ def load_library(path=LIB_PATH):
         "eagle_status_string": (ctypes.c_char_p, [I]),
         "eagle_version": (I, []),
         "eagle_draft_topk_workspace_size": (SZ, [I, I, I, I]),
-        "eagle_draft_topk": (I, [P, I, I, I, I, I, I64, P, P, P, P, SZ, P]),
+        "eagle_draft_topk": (I, [P, I, I, I, I, I, I64, P, P, P, P, P, SZ, P]),
         "eagle_tree_build": (I, [P, P, I, I, I, I, P, P, P, P, P, P, P, P, P, P]),
         "eagle_tree_mask": (I, [P, I, I, P, P]),
         "eagle_tree_attn_workspace_size": (SZ, [I, I, I, I, I, I, I]),
@@ -111,7 +111,8 @@ class Workspace:
         return self.buf, self.buf.numel()
 
 
-def draft_topk(logits, k, tok=None, conf=None, stats=None, workspace=None, stream=None):
+def draft_topk(logits, k, tok=None, conf=None, stats=None, workspace=None, status=None,
+               stream=None):
     """logits [B, D, k, V(ld)] -> tok int32 [B,D,k,k], conf f32, stats f32 [B,D,k,2]."""
     lib = load_library()
     _cuda(logits, "logits")
@@ -128,7 +129,8 @@ def draft_topk(logits, k, tok=None, conf=None, stats=None, workspace=None, strea
     ws = workspace or Workspace(dev)
     wbuf, wbytes = ws.get(lib.eagle_draft_topk_workspace_size(B, D, k, V))
     _check(lib.eagle_draft_topk(_ptr(logits), _dtype_code(logits), B, D, k, V, ld, _ptr(tok),
-                                _ptr(conf), _ptr(stats), _ptr(wbuf), wbytes, _stream(stream)),
+                                _ptr(conf), _ptr(stats), _ptr(status), _ptr(wbuf), wbytes,
+                                _stream(stream)),
            "eagle_draft_topk")
     return tok, conf, stats
 

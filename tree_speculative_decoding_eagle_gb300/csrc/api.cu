@@ -9,8 +9,8 @@ namespace eagle {
 // draft_topk.cu
 size_t draft_workspace_bytes(int B, int D, int k, int V, int vec, int num_sms);
 cudaError_t launch_draft_topk(const void *logits, int dtype, int B, int D, int k, int V, int64_t ld,
-                              int32_t *tok, float *conf, float *stats, void *ws, int num_sms,
-                              cudaStream_t st);
+                              int32_t *tok, float *conf, float *stats, void *ws, int32_t *status,
+                              int num_sms, cudaStream_t st);
 // tree_build.cu
 cudaError_t launch_tree_build(const int32_t *tok, const float *conf, int B, int D, int k, int m,
                               const int32_t *root_tok, int32_t *node_tok, int32_t *node_parent,
@@ -80,7 +80,7 @@ size_t eagle_draft_topk_workspace_size(int B, int D, int k, int V) {
 }
 
 int eagle_draft_topk(const void *logits, int dtype, int B, int D, int k, int V, int64_t ld,
-                     int32_t *tok, float *conf, float *stats, void *workspace,
+                     int32_t *tok, float *conf, float *stats, int32_t *status, void *workspace,
                      size_t workspace_bytes, eagle_stream_t stream) {
   if (!logits || !tok || !conf || !valid_dtype(dtype)) return EAGLE_ERR_INVALID;
   if (B < 1 || D < 1 || k < 1 || k > 32 || V < 1 || k > V || ld < V) return EAGLE_ERR_INVALID;
@@ -91,7 +91,7 @@ int eagle_draft_topk(const void *logits, int dtype, int B, int D, int k, int V, 
   const size_t need = draft_workspace_bytes(B, D, k, V, 16 / es, sms);
   if (workspace_bytes < need || (need && !workspace)) return EAGLE_ERR_WORKSPACE;
   return from_cuda(launch_draft_topk(logits, dtype, B, D, k, V, ld, tok, conf, stats, workspace,
-                                     sms, reinterpret_cast<cudaStream_t>(stream)));
+                                     status, sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int eagle_tree_build(const int32_t *tok, const float *conf, int B, int D, int k, int m,

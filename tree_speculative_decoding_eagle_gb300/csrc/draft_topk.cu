@@ -6,13 +6,21 @@
 // token id) and c = exp(x - M) / Z.
 //
 // One pass over HBM.  A row may be split across S CTAs (to fill the GPU when
-// there are few rows); each CTA streams its slice with 16-byte vector loads,
-// keeps an online (max, sum-exp) pair and a per-thread top-K list of unique
-// 64-bit keys (logit order, then lower token id), merges them warp-wide with
-// bitonic shuffles and block-wide through shared memory.  With S > 1 the last
-// CTA of a row to finish (atomic ticket in the workspace) merges the S
-// partial results; no CTA ever waits for another.
+// there are few rows); each CTA streams its slice through a ring of shared-
+// memory stages filled by bulk copies and keeps an online (max, sum-exp) pair
+// per thread.  Top-k selection works on unique 64-bit keys (logit order, then
+// lower token id).  Every lane tracks its running maximum; the k-th largest
+// lane maximum of a warp (a 32-lane bitonic sort per chunk) bounds the top k
+// from below, and the block keeps the largest such bound.  Values at or
+// above the bound are appended to a per-warp shared-memory buffer by a
+// ballot scan, so only about k candidates per warp survive; the buffer is
+// merged into the warp's top-K list (register insertion plus bitonic
+// shuffles) when full and at the end.  Warp lists
+// merge block-wide through shared memory.  With S > 1 the last CTA of a row
+// to finish (atomic ticket in the workspace) merges the S partial results;
+// no CTA ever waits for another.
 #include "common.cuh"
+#include "sm100.cuh"
 
 namespace eagle {
 
@@ -24,10 +32,14 @@ struct DraftArgs {
   float *conf;
   float *stats;
   unsigned char *ws;     // [counters (B*R u32, 256-aligned)][records]
+  int32_t *status;
 };
 
 constexpr int kDraftThreads = 256;
-constexpr int kDraftUnroll = 4;
+constexpr int kDraftUnroll = 4;                                // vectors per thread per chunk
+constexpr int kDraftChunkVec = kDraftThreads * kDraftUnroll;   // 16-byte vectors per chunk
+constexpr int kDraftStages = 4;                                // chunks in flight per CTA
+constexpr int kDraftSmem = kDraftStages * kDraftChunkVec * 16 + 128;
 
 template <int K>
 struct alignas(16) DraftPartial {
@@ -38,11 +50,6 @@ struct alignas(16) DraftPartial {
 
 __host__ __device__ inline size_t draft_counter_bytes(int B, int R) {
   return (static_cast<size_t>(B) * R * sizeof(uint32_t) + 255) / 256 * 256;
-}
-
-template <int K>
-__device__ __forceinline__ float list_floor(const uint64_t (&list)[K]) {
-  return list[K - 1] ? key_value(list[K - 1]) : -INFINITY;
 }
 
 // Write the k best keys of a finished row (all lanes of the calling warp hold
@@ -72,70 +79,188 @@ __device__ __forceinline__ void draft_finalize(const DraftArgs &a, int b, int d,
   }
 }
 
+// Bitonic sort of one float per lane across the warp, descending by lane.
+__device__ __forceinline__ float warp_sort_desc(float x, int lane) {
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const float y = __shfl_xor_sync(0xffffffffu, x, stride);
+      const bool desc = (lane & size) == 0;
+      const bool lower = (lane & stride) == 0;
+      x = (desc == lower) ? fmaxf(x, y) : fminf(x, y);
+    }
+  }
+  return x;
+}
+
+// Merge the warp's candidate buffer into the warp list (held identically by
+// every lane); afterwards every lane again holds the warp's top K.
+template <int K>
+__device__ __forceinline__ void draft_flush(uint64_t (&list)[K], const uint64_t *buf, int fill,
+                                            int lane) {
+  __syncwarp();
+  if (lane != 0) {
+#pragma unroll
+    for (int q = 0; q < K; ++q) list[q] = 0;
+  }
+  for (int i = lane; i < fill; i += 32) list_insert<K>(list, buf[i]);
+  warp_topk<K>(list);
+  __syncwarp();
+}
+
 template <typename T, int K>
 __global__ void __launch_bounds__(kDraftThreads) draft_topk_kernel(DraftArgs a) {
   using VT = VecTraits<T>;
   constexpr int VEC = VT::kElems;
+  constexpr int BUF = 32 * VEC;  // one full vector step of the warp always fits
+  __shared__ uint64_t s_buf[kDraftThreads / 32][2 * BUF];
   const int s = blockIdx.x;
   const int rg = blockIdx.y;  // b * R + r
   const int b = rg / a.R, r = rg % a.R;
   const int d = r == 0 ? 0 : 1 + (r - 1) / a.k;
   const int j = r == 0 ? 0 : (r - 1) % a.k;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint64_t *buf = s_buf[warp];
 
   const T *row = reinterpret_cast<const T *>(a.logits) +
                  ((static_cast<int64_t>(b) * a.D + d) * a.k + j) * a.ld;
   const int64_t NV = a.V / VEC;
   const int64_t v0 = NV * s / a.S, v1 = NV * (s + 1) / a.S;
+  const int n_chunks = static_cast<int>((v1 - v0 + kDraftChunkVec - 1) / kDraftChunkVec);
+
+  // the slice streams through a ring of shared-memory stages filled by bulk
+  // copies (one elected thread), so many bytes are in flight per SM
+  extern __shared__ __align__(128) unsigned char dsm[];
+  uint4 *stage_buf = reinterpret_cast<uint4 *>(dsm);
+  uint64_t *full = reinterpret_cast<uint64_t *>(dsm + kDraftStages * kDraftChunkVec * 16);
+  __shared__ volatile int s_abort;
+  __shared__ unsigned s_thr;  // block prune bound (order-preserving bits)
+  if (tid == 0) {
+    s_abort = 0;
+    s_thr = ordered_u32(-INFINITY);
+    for (int q = 0; q < kDraftStages; ++q) sm100::mbar_init(&full[q], 1);
+    sm100::mbar_init_fence();
+  }
+  __syncthreads();
+  auto issue = [&](int c) {
+    const int64_t first = v0 + static_cast<int64_t>(c) * kDraftChunkVec;
+    const uint32_t nvec = static_cast<uint32_t>(min(static_cast<int64_t>(kDraftChunkVec), v1 - first));
+    uint64_t *bar = &full[c % kDraftStages];
+    sm100::mbar_arrive_expect_tx(bar, nvec * 16u);
+    sm100::bulk_load(stage_buf + (c % kDraftStages) * kDraftChunkVec, row + first * VEC, nvec * 16u, bar);
+  };
+  if (tid == 0)
+    for (int c = 0; c < min(kDraftStages, n_chunks); ++c) issue(c);
 
   float m = -INFINITY, sum = 0.f;
-  uint64_t list[K];
+  uint64_t list[K];  // the warp's top K so far, identical in every lane
 #pragma unroll
   for (int q = 0; q < K; ++q) list[q] = 0;
-  float thr = -INFINITY, wthr = -INFINITY;
+  float lmax = -INFINITY;  // this lane's largest value so far
+  float thr = -INFINITY;   // prune bound: at least k values of the slice are >= thr
+  int fill = 0;            // candidates waiting in the warp buffer
+  int consumed = 0;
 
-  for (int64_t base = v0; base < v1; base += kDraftThreads * kDraftUnroll) {
-    uint4 buf[kDraftUnroll];
+  for (int c = 0; c < n_chunks; ++c) {
+    const int st = c % kDraftStages;
+    if (!sm100::mbar_wait(&full[st], (c / kDraftStages) & 1, &s_abort)) report(a.status, EAGLE_ERR_TIMEOUT);
+    const int64_t first = v0 + static_cast<int64_t>(c) * kDraftChunkVec;
+    const int nvec = static_cast<int>(min(static_cast<int64_t>(kDraftChunkVec), v1 - first));
+    const uint4 *src = stage_buf + st * kDraftChunkVec;
+    uint4 vb[kDraftUnroll];
+    float vmx[kDraftUnroll];
 #pragma unroll
     for (int u = 0; u < kDraftUnroll; ++u) {
-      int64_t idx = base + u * kDraftThreads + tid;
-      if (idx < v1) buf[u] = ld_stream16(row + idx * VEC);
-    }
-#pragma unroll
-    for (int u = 0; u < kDraftUnroll; ++u) {
-      int64_t idx = base + u * kDraftThreads + tid;
-      if (idx < v1) {
+      const int iv = u * kDraftThreads + tid;
+      vmx[u] = -INFINITY;
+      if (iv < nvec && !s_abort) {
+        vb[u] = src[iv];
         float x[VEC];
-        VT::unpack(buf[u], x);
+        VT::unpack(vb[u], x);
         float vmax = x[0];
 #pragma unroll
         for (int e = 1; e < VEC; ++e) vmax = fmaxf(vmax, x[e]);
+        vmx[u] = vmax;
         if (vmax > -INFINITY) {
           if (vmax > m) {
             sum *= ex2_approx((m - vmax) * kLog2e);
             m = vmax;
           }
           const float mL = m * kLog2e;
+          float p[VEC];
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) sum += ex2_approx(fmaf(x[e], kLog2e, -mL));
-          if (vmax > thr && vmax >= wthr) {
-            const uint32_t t0 = static_cast<uint32_t>(idx * VEC);
+          for (int e = 0; e < VEC; ++e) p[e] = ex2_approx(fmaf(x[e], kLog2e, -mL));
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-              if (x[e] > thr && x[e] >= wthr) {
-                list_insert<K>(list, topk_key(x[e], t0 + e));
-                thr = list_floor<K>(list);
-              }
-            }
-          }
+          for (int w2 = VEC / 2; w2 > 0; w2 >>= 1)  // pairwise within the vector
+#pragma unroll
+            for (int e = 0; e < w2; ++e) p[e] += p[e + w2];
+          sum += p[0];
         }
+        lmax = fmaxf(lmax, vmax);
       }
     }
-    wthr = from_ordered_u32(__reduce_max_sync(0xffffffffu, ordered_u32(thr)));
+    // Lane maxima are distinct elements, so the k-th largest of the warp's
+    // lane maxima has at least k elements at or above it; so has any other
+    // warp's bound, and the block keeps the largest of them.
+    {
+      float y = warp_sort_desc(lmax, lane);
+      const float tw = __shfl_sync(0xffffffffu, y, a.k - 1);
+      if (tw > -INFINITY) atomicMax(&s_thr, ordered_u32(tw));
+      thr = fmaxf(thr, fmaxf(tw, from_ordered_u32(s_thr)));
+    }
+#pragma unroll
+    for (int u = 0; u < kDraftUnroll; ++u) {
+      const int iv = u * kDraftThreads + tid;
+      const bool maybe = vmx[u] > -INFINITY && vmx[u] >= thr;
+      if (__any_sync(0xffffffffu, maybe)) {
+        unsigned cm = 0;
+        float x[VEC];
+        VT::unpack(vb[u], x);
+        if (maybe) {
+#pragma unroll
+          for (int e = 0; e < VEC; ++e)
+            if (x[e] >= thr && x[e] > -INFINITY) cm |= 1u << e;
+        }
+        const int cnt = __popc(cm);
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        const int total = __shfl_sync(0xffffffffu, incl, 31);
+        if (fill + total > 2 * BUF) {
+          draft_flush<K>(list, buf, fill, lane);
+          fill = 0;
+        }
+        if (cm) {
+          int pos = fill + incl - cnt;
+          const uint32_t t0 = static_cast<uint32_t>((first + iv) * VEC);
+#pragma unroll
+          for (int e = 0; e < VEC; ++e)
+            if ((cm >> e) & 1u) buf[pos++] = topk_key(x[e], t0 + e);
+        }
+        fill += total;
+      }
+    }
+    consumed = c + 1;
+    __syncthreads();  // every thread is done with this stage
+    if (s_abort) break;
+    if (tid == 0 && c + kDraftStages < n_chunks) issue(c + kDraftStages);
   }
+  if (s_abort) {
+    // drain the copies still in flight before the CTA's shared memory goes away
+    if (tid == 0) {
+      volatile int never = 0;
+      for (int c = max(0, consumed - 1); c < min(n_chunks, consumed - 1 + kDraftStages); ++c)
+        sm100::mbar_wait(&full[c % kDraftStages], (c / kDraftStages) & 1, &never, 100000000ull);
+    }
+    return;
+  }
+  if (fill > 0) draft_flush<K>(list, buf, fill, lane);
 
-  // ---- warp merge -------------------------------------------------------
-  warp_topk<K>(list);
+  // ---- warp statistics ------------------------------------------------------
   {
     float mw = warp_max(m);
     float sw = (m == -INFINITY) ? 0.f : sum * ex2_approx((m - mw) * kLog2e);
@@ -220,7 +345,7 @@ static int draft_kpow2(int k) {
 int draft_splits(int B, int R, int V, int vec, int num_sms) {
   const int64_t rows = static_cast<int64_t>(B) * R;
   const int64_t NV = V / vec;
-  const int64_t target = static_cast<int64_t>(num_sms) * 8;
+  const int64_t target = static_cast<int64_t>(num_sms) * 2;  // two CTAs fit per SM
   int64_t S = (target + rows - 1) / rows;
   // keep at least two full vector sweeps of the block per split
   int64_t max_by_len = NV / (2 * kDraftThreads);
@@ -239,25 +364,35 @@ size_t draft_workspace_bytes(int B, int D, int k, int V, int vec, int num_sms) {
   return draft_counter_bytes(B, R) + (S > 1 ? static_cast<size_t>(B) * R * S * rec : 0);
 }
 
+template <typename T, int K>
+static cudaError_t launch_tk(const DraftArgs &a, cudaStream_t st) {
+  static bool configured = false;  // the attribute is per function, set once
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(draft_topk_kernel<T, K>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kDraftSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  draft_topk_kernel<T, K><<<dim3(a.S, a.B * a.R), kDraftThreads, kDraftSmem, st>>>(a);
+  return cudaGetLastError();
+}
+
 template <typename T>
 static cudaError_t launch_t(const DraftArgs &a, cudaStream_t st) {
-  dim3 grid(a.S, a.B * a.R);
-  const int K = draft_kpow2(a.k);
-  switch (K) {
-    case 1: draft_topk_kernel<T, 1><<<grid, kDraftThreads, 0, st>>>(a); break;
-    case 2: draft_topk_kernel<T, 2><<<grid, kDraftThreads, 0, st>>>(a); break;
-    case 4: draft_topk_kernel<T, 4><<<grid, kDraftThreads, 0, st>>>(a); break;
-    case 8: draft_topk_kernel<T, 8><<<grid, kDraftThreads, 0, st>>>(a); break;
-    case 16: draft_topk_kernel<T, 16><<<grid, kDraftThreads, 0, st>>>(a); break;
-    case 32: draft_topk_kernel<T, 32><<<grid, kDraftThreads, 0, st>>>(a); break;
+  switch (draft_kpow2(a.k)) {
+    case 1: return launch_tk<T, 1>(a, st);
+    case 2: return launch_tk<T, 2>(a, st);
+    case 4: return launch_tk<T, 4>(a, st);
+    case 8: return launch_tk<T, 8>(a, st);
+    case 16: return launch_tk<T, 16>(a, st);
+    case 32: return launch_tk<T, 32>(a, st);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_draft_topk(const void *logits, int dtype, int B, int D, int k, int V,
                               int64_t ld, int32_t *tok, float *conf, float *stats,
-                              void *ws, int num_sms, cudaStream_t st) {
+                              void *ws, int32_t *status, int num_sms, cudaStream_t st) {
   DraftArgs a;
   a.logits = logits;
   a.B = B; a.D = D; a.k = k; a.V = V; a.ld = ld;
@@ -266,6 +401,7 @@ cudaError_t launch_draft_topk(const void *logits, int dtype, int B, int D, int k
   a.S = draft_splits(B, a.R, V, vec, num_sms);
   a.tok = tok; a.conf = conf; a.stats = stats;
   a.ws = reinterpret_cast<unsigned char *>(ws);
+  a.status = status;
   return dtype == EAGLE_BF16 ? launch_t<__nv_bfloat16>(a, st) : launch_t<float>(a, st);
 }
 
