@@ -171,8 +171,14 @@ int eagle_tree_mask(const int32_t *node_parent, int B, int n, uint64_t *mask,
  *   mask       device uint64 [B, n, ceil(n/64)] (as eagle_tree_mask writes)
  *   out        [B, n, Hq, dh]        dtype   (out)
  *   lse        device float [B, n, Hq]  (out; may be NULL)
- * Arithmetic: fp32 accumulation and softmax; bf16 inputs use the tensor
- * cores.  Limits: Hq % Hkv == 0, dh in {64, 128}, 1 <= n <= 4096.
+ *   status     device int32 (out; may be NULL): EAGLE_ERR_TIMEOUT if a
+ *              bounded wait inside the kernel gave up
+ * Arithmetic: fp32 accumulation and softmax.  bf16 inputs run on the tensor
+ * cores (tcgen05, operands staged by TMA, accumulators in tensor memory,
+ * probabilities rounded to bf16 for the P.V product); fp32 inputs run on the
+ * CUDA cores.  Cache rows at or beyond kv_len[b] are never read; every row
+ * of k_tree / v_tree must hold finite values.
+ * Limits: Hq % Hkv == 0, dh in {64, 128}, 1 <= n <= 4096, B*Hkv <= 65535.
  * ------------------------------------------------------------------------ */
 size_t eagle_tree_attn_workspace_size(int dtype, int B, int n, int Hq, int Hkv,
                                       int dh, int Lmax);
@@ -181,7 +187,7 @@ int eagle_tree_attn(const void *q, const void *k_cache, const void *v_cache,
                     const int32_t *kv_len, const void *k_tree,
                     const void *v_tree, const uint64_t *mask, int dtype, int B,
                     int n, int Hq, int Hkv, int dh, int Lmax, float scale,
-                    void *out, float *lse, void *workspace,
+                    void *out, float *lse, int32_t *status, void *workspace,
                     size_t workspace_bytes, eagle_stream_t stream);
 
 /* ------------------------------------------------------------------------

@@ -67,7 +67,7 @@ def test_invalid_arguments_are_rejected_on_the_host(lib):
     assert lib.eagle_tree_mask(fake, 1, 0, fake, NULL) == -1
     assert lib.eagle_tree_mask(fake, 1, 5000, fake, NULL) == -1
     # tree_attn: Hq not a multiple of Hkv, unsupported head dim
-    a = [fake] * 7 + [1, 1, 3, 6, 4, 64, 16, ctypes.c_float(0.1), fake, NULL, NULL, 0, NULL]
+    a = [fake] * 7 + [1, 1, 3, 6, 4, 64, 16, ctypes.c_float(0.1), fake, NULL, NULL, NULL, 0, NULL]
     assert lib.eagle_tree_attn(*a) == -1
     a[10], a[11], a[12] = 8, 4, 96
     assert lib.eagle_tree_attn(*a) == -2

@@ -55,7 +55,7 @@ def load_library(path=LIB_PATH):
         "eagle_tree_build": (I, [P, P, I, I, I, I, P, P, P, P, P, P, P, P, P, P]),
         "eagle_tree_mask": (I, [P, I, I, P, P]),
         "eagle_tree_attn_workspace_size": (SZ, [I, I, I, I, I, I, I]),
-        "eagle_tree_attn": (I, [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, P, P, SZ, P]),
+        "eagle_tree_attn": (I, [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, P, P, P, SZ, P]),
         "eagle_verify_workspace_size": (SZ, [I, I, I]),
         "eagle_verify": (I, [P, I, I64, P, P, I, I, I, I, I, F, P, P, P, P, P, P, SZ, P]),
     }
@@ -171,7 +171,7 @@ def tree_mask(node_parent, mask=None, stream=None):
 
 
 def tree_attn(q, k_cache, v_cache, kv_len, k_tree, v_tree, mask, scale=None, out=None,
-              lse=None, workspace=None, stream=None):
+              lse=None, workspace=None, status=None, stream=None):
     """q [B,n,Hq,dh], caches [B,Hkv,Lmax,dh], tree KV [B,Hkv,n,dh] -> out, lse."""
     lib = load_library()
     for t, nm in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (k_tree, "k_tree"),
@@ -189,8 +189,8 @@ def tree_attn(q, k_cache, v_cache, kv_len, k_tree, v_tree, mask, scale=None, out
     wbuf, wbytes = ws.get(lib.eagle_tree_attn_workspace_size(dt, B, n, Hq, Hkv, dh, Lmax))
     _check(lib.eagle_tree_attn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), _ptr(k_tree),
                                _ptr(v_tree), _ptr(mask), dt, B, n, Hq, Hkv, dh, Lmax,
-                               ctypes.c_float(scale), _ptr(out), _ptr(lse), _ptr(wbuf), wbytes,
-                               _stream(stream)), "eagle_tree_attn")
+                               ctypes.c_float(scale), _ptr(out), _ptr(lse), _ptr(status),
+                               _ptr(wbuf), wbytes, _stream(stream)), "eagle_tree_attn")
     return out, lse
 
 

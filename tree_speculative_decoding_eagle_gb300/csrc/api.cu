@@ -24,6 +24,11 @@ cudaError_t launch_tree_attn_simt(const void *q, const void *k_cache, const void
                                   const uint64_t *mask, int dtype, int B, int n, int Hq, int Hkv,
                                   int dh, int Lmax, float scale, void *out, float *lse, void *ws,
                                   int num_sms, cudaStream_t st);
+size_t attn_tc_workspace_bytes(int B, int n, int Hq, int Hkv, int dh, int Lmax, int num_sms);
+cudaError_t launch_tree_attn_tc(const void *q, const void *k_cache, const void *v_cache, const int32_t *kv_len,
+                                const void *k_tree, const void *v_tree, const uint64_t *mask, int B, int n,
+                                int Hq, int Hkv, int dh, int Lmax, float scale, void *out, float *lse, void *ws,
+                                int32_t *status, int num_sms, cudaStream_t st);
 // verify.cu
 size_t verify_workspace_bytes(int B, int m, int V);
 cudaError_t launch_verify(const void *target, int dtype, int64_t ld, const int32_t *node_tok,
@@ -113,28 +118,35 @@ int eagle_tree_mask(const int32_t *node_parent, int B, int n, uint64_t *mask, ea
 }
 
 size_t eagle_tree_attn_workspace_size(int dtype, int B, int n, int Hq, int Hkv, int dh, int Lmax) {
-  (void)dtype; (void)Hkv;
-  if (B < 1 || n < 1 || Hq < 1 || dh < 1 || Lmax < 0) return 0;
+  if (B < 1 || n < 1 || Hq < 1 || Hkv < 1 || dh < 1 || Lmax < 0) return 0;
+  if (dtype == EAGLE_BF16) return attn_tc_workspace_bytes(B, n, Hq, Hkv, dh, Lmax, current_num_sms());
   return attn_simt_workspace_bytes(B, n, Hq, dh, Lmax, current_num_sms());
 }
 
 int eagle_tree_attn(const void *q, const void *k_cache, const void *v_cache, const int32_t *kv_len,
                     const void *k_tree, const void *v_tree, const uint64_t *mask, int dtype, int B,
                     int n, int Hq, int Hkv, int dh, int Lmax, float scale, void *out, float *lse,
-                    void *workspace, size_t workspace_bytes, eagle_stream_t stream) {
+                    int32_t *status, void *workspace, size_t workspace_bytes, eagle_stream_t stream) {
   if (!q || !k_cache || !v_cache || !kv_len || !k_tree || !v_tree || !mask || !out) return EAGLE_ERR_INVALID;
   if (!valid_dtype(dtype) || B < 1 || n < 1 || n > 4096 || Hq < 1 || Hkv < 1 || Hq % Hkv || Lmax < 0)
     return EAGLE_ERR_INVALID;
   if (dh != 64 && dh != 128) return EAGLE_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(B) * Hkv > 65535) return EAGLE_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_tree) ||
       !aligned16(v_tree) || !aligned16(out))
     return EAGLE_ERR_INVALID;
   const int sms = current_num_sms();
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == EAGLE_BF16) {
+    const size_t need = attn_tc_workspace_bytes(B, n, Hq, Hkv, dh, Lmax, sms);
+    if (workspace_bytes < need || (need && !workspace)) return EAGLE_ERR_WORKSPACE;
+    return from_cuda(launch_tree_attn_tc(q, k_cache, v_cache, kv_len, k_tree, v_tree, mask, B, n, Hq, Hkv, dh,
+                                         Lmax, scale, out, lse, workspace, status, sms, st));
+  }
   const size_t need = attn_simt_workspace_bytes(B, n, Hq, dh, Lmax, sms);
   if (workspace_bytes < need || (need && !workspace)) return EAGLE_ERR_WORKSPACE;
-  return from_cuda(launch_tree_attn_simt(q, k_cache, v_cache, kv_len, k_tree, v_tree, mask, dtype, B,
-                                         n, Hq, Hkv, dh, Lmax, scale, out, lse, workspace, sms,
-                                         reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(launch_tree_attn_simt(q, k_cache, v_cache, kv_len, k_tree, v_tree, mask, dtype, B, n, Hq,
+                                         Hkv, dh, Lmax, scale, out, lse, workspace, sms, st));
 }
 
 size_t eagle_verify_workspace_size(int B, int m, int V) {

@@ -64,6 +64,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
   }
 }
 
+// Warp-uniform wait: lane 0 polls, every lane gets the same answer.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+  bool ok = false;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort);
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
 // ---- proxy fences --------------------------------------------------------------
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (tensor cores, TMA).

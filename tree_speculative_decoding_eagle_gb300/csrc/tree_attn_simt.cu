@@ -169,6 +169,23 @@ static cudaError_t launch_simt_t(AttnArgs a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// Split-KV merge for the tensor-core path (bf16 output, same partial layout).
+cudaError_t launch_attn_combine_bf16(const float *part_o, const float *part_ml, int B, int n, int Hq, int dh,
+                                     int S, void *out, float *lse, cudaStream_t st) {
+  AttnArgs a = {};
+  a.B = B; a.n = n; a.Hq = Hq; a.dh = dh; a.S = S;
+  a.out = out; a.lse = lse;
+  a.part_o = const_cast<float *>(part_o);
+  a.part_ml = const_cast<float *>(part_ml);
+  const int64_t rows = static_cast<int64_t>(B) * n * Hq;
+  const int grid = static_cast<int>((rows * 32 + 255) / 256);
+  if (dh == 64)
+    attn_combine_kernel<__nv_bfloat16, 64><<<grid, 256, 0, st>>>(a);
+  else
+    attn_combine_kernel<__nv_bfloat16, 128><<<grid, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_tree_attn_simt(const void *q, const void *k_cache, const void *v_cache,
                                   const int32_t *kv_len, const void *k_tree, const void *v_tree,
                                   const uint64_t *mask, int dtype, int B, int n, int Hq, int Hkv,

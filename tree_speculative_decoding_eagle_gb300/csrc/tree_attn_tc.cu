@@ -1,0 +1,497 @@
+// Stage 3 (tensor-core path, bf16): tree-masked attention of the tree nodes
+// over the KV prefix on the 5th-generation tensor cores.
+//
+// [EAGLE-1] sections "用語解説" (Tree Attention) and "Tree Attention の役割":
+// the target scores every branch of the draft tree in one forward pass; with
+// the [EAGLE-2] mask (section "注意マスクの調整") node i attends to the
+// prefix and to its own ancestors only.
+//
+// One CTA per (sequence b, KV head g, group of MT M-tiles, KV split).  Query
+// rows are (node, head-in-group) pairs, so the m+1 nodes x G grouped heads of
+// a KV head share every K/V tile.  Key tiles are 64 keys: first the prefix
+// (positions 0..kv_len-1), then the tree nodes, whose tile is masked with the
+// ancestor bits.  Roles:
+//   * producer warp: K/V tiles into a ring of shared-memory stages, by TMA
+//     (128-byte swizzle) for full tiles, by plain loads with zero fill for
+//     the ragged last prefix tile;
+//   * MMA warp (one elected thread): S_t = Q_t K^T and O_t += P_t V with
+//     tcgen05.mma, accumulators in tensor memory, completion via
+//     tcgen05.commit on mbarriers;
+//   * one softmax warpgroup per M-tile: reads its S rows from tensor memory,
+//     online softmax in fp32 (base-2), writes P (bf16) to swizzled shared
+//     memory, rescales its O rows in tensor memory when the row max grows.
+// Every wait is bounded; a timeout raises EAGLE_ERR_TIMEOUT in the status
+// word and the CTA drains its copies and MMAs, frees tensor memory and exits.
+#include <mutex>
+
+#include "common.cuh"
+#include "sm100.cuh"
+
+namespace eagle {
+
+using namespace sm100;
+
+constexpr int kNK = 64;  // keys per tile
+
+struct TcArgs {
+  const __nv_bfloat16 *q, *k_cache, *v_cache;
+  const int32_t *kv_len;
+  const uint64_t *mask;
+  int B, n, Hq, Hkv, G, Lmax, S, W;
+  float scale_log2;  // softmax scale times log2(e)
+  __nv_bfloat16 *out;
+  float *lse;
+  float *part_o, *part_ml;
+  int32_t *status;
+};
+
+template <int DH, int MT, int STAGES>
+struct TcShape {
+  static constexpr int kRegions = DH / 64;
+  static constexpr int kQBytes = MT * kRegions * 16384;
+  static constexpr int kPBytes = MT * 16384;
+  static constexpr int kTileBytes = kRegions * 8192;        // one K (or V) tile
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kBarOff = kQBytes + kPBytes + STAGES * kStageBytes;
+  static constexpr int kNumBars = 2 * STAGES + 4 * MT + 1;
+  static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;  // + alignment slack
+  static constexpr int kThreads = MT * 128 + 64;
+  static constexpr int kTmemCols = MT * (kNK + DH) <= 128 ? 128 : (MT * (kNK + DH) <= 256 ? 256 : 512);
+};
+
+template <int DH, int MT, int STAGES>
+__global__ void __launch_bounds__(MT * 128 + 64, 1)
+    tree_attn_tc_kernel(const __grid_constant__ CUtensorMap kc_map, const __grid_constant__ CUtensorMap vc_map,
+                        const __grid_constant__ CUtensorMap kt_map, const __grid_constant__ CUtensorMap vt_map,
+                        TcArgs a) {
+  using Sh = TcShape<DH, MT, STAGES>;
+  extern __shared__ unsigned char raw_smem[];
+  unsigned char *sm = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(raw_smem) + 1023) & ~static_cast<uintptr_t>(1023));
+  unsigned char *sQ = sm;
+  unsigned char *sP = sm + Sh::kQBytes;
+  unsigned char *sKV = sP + Sh::kPBytes;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + Sh::kBarOff);
+  uint64_t *kv_full = bars;
+  uint64_t *kv_empty = bars + STAGES;
+  uint64_t *s_full = bars + 2 * STAGES;
+  uint64_t *s_free = s_full + MT;
+  uint64_t *p_full = s_free + MT;
+  uint64_t *o_done = p_full + MT;
+  uint64_t *teardown = o_done + MT;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Sh::kNumBars);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int split = blockIdx.x, mg = blockIdx.y;
+  const int bg = blockIdx.z, b = bg / a.Hkv, g = bg % a.Hkv;
+  const int n = a.n;
+  const int L = min(max(a.kv_len[b], 0), a.Lmax);
+  const int n_ptiles = (L + kNK - 1) / kNK;
+  const int tps = (n_ptiles + a.S - 1) / a.S;
+  const int p0 = min(n_ptiles, split * tps), p1 = min(n_ptiles, p0 + tps);
+  const int np = p1 - p0;
+  const int ntt = (split == a.S - 1) ? (n + kNK - 1) / kNK : 0;
+  const int T = np + ntt;  // key tiles of this CTA
+  const int producer_warp = MT * 4, mma_warp = MT * 4 + 1;
+
+  // ---- Q tiles -> shared memory (zero rows beyond the last node) ----------
+  const int rows_total = n * a.G;
+  for (int idx = tid; idx < MT * 128 * (DH / 8); idx += Sh::kThreads) {
+    const int t = idx / (128 * (DH / 8));
+    const int rem = idx % (128 * (DH / 8));
+    const int r = rem / (DH / 8), c = rem % (DH / 8);
+    const int rho = (mg * MT + t) * 128 + r;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (rho < rows_total) {
+      const int i = rho / a.G, hh = rho % a.G;
+      const __nv_bfloat16 *src = a.q + ((static_cast<int64_t>(b) * n + i) * a.Hq + g * a.G + hh) * DH;
+      v = *reinterpret_cast<const uint4 *>(src + c * 8);
+    }
+    *reinterpret_cast<uint4 *>(sQ + (t * Sh::kRegions + c / 8) * 16384 + sw128_offset(r, c % 8)) = v;
+  }
+  fence_async_smem();
+  if (tid == 0) {
+    for (int q = 0; q < STAGES; ++q) {
+      mbar_init(&kv_full[q], 1);
+      mbar_init(&kv_empty[q], 1);
+    }
+    for (int t = 0; t < MT; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&s_free[t], 4);
+      mbar_init(&p_full[t], 4);
+      mbar_init(&o_done[t], 1);
+    }
+    mbar_init(teardown, 1);
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == mma_warp) {
+    tmem_alloc(tmem_slot, Sh::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  int issued = 0;  // producer: tiles issued
+
+  if (warp == producer_warp) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      prefetch_tmap(&kc_map);
+      prefetch_tmap(&vc_map);
+      prefetch_tmap(&kt_map);
+      prefetch_tmap(&vt_map);
+    }
+    for (int j = 0; j < T; ++j) {
+      const int st = j % STAGES, use = j / STAGES;
+      if (use >= 1 && !warp_wait(&kv_empty[st], (use - 1) & 1, abort_flag)) break;
+      unsigned char *kst = sKV + st * Sh::kStageBytes;
+      unsigned char *vst = kst + Sh::kTileBytes;
+      const bool prefix = j < np;
+      const int key0 = prefix ? (p0 + j) * kNK : (j - np) * kNK;
+      const int valid = prefix ? min(kNK, L - key0) : kNK;
+      if (!prefix || valid == kNK) {
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&kv_full[st], Sh::kStageBytes);
+          const CUtensorMap *km = prefix ? &kc_map : &kt_map;
+          const CUtensorMap *vm = prefix ? &vc_map : &vt_map;
+          const int row0 = prefix ? bg * a.Lmax + key0 : bg * n + key0;
+#pragma unroll
+          for (int r = 0; r < Sh::kRegions; ++r) {
+            tma_load_2d(kst + r * 8192, km, r * 64, row0, &kv_full[st]);
+            tma_load_2d(vst + r * 8192, vm, r * 64, row0, &kv_full[st]);
+          }
+        }
+      } else {
+        // ragged last prefix tile: rows >= valid are zero (cache memory past
+        // kv_len is never read)
+        const __nv_bfloat16 *kg = a.k_cache + (static_cast<int64_t>(bg) * a.Lmax + key0) * DH;
+        const __nv_bfloat16 *vg = a.v_cache + (static_cast<int64_t>(bg) * a.Lmax + key0) * DH;
+        for (int idx = lane; idx < kNK * (DH / 8); idx += 32) {
+          const int r = idx / (DH / 8), c = idx % (DH / 8);
+          uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+          if (r < valid) {
+            kv = *reinterpret_cast<const uint4 *>(kg + r * DH + c * 8);
+            vv = *reinterpret_cast<const uint4 *>(vg + r * DH + c * 8);
+          }
+          const uint32_t off = (c / 8) * 8192 + sw128_offset(r, c % 8);
+          *reinterpret_cast<uint4 *>(kst + off) = kv;
+          *reinterpret_cast<uint4 *>(vst + off) = vv;
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&kv_full[st]);
+      }
+      issued = j + 1;
+    }
+  } else if (warp == mma_warp) {
+    // --------------------------------------------------------------------- MMA
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16(128, kNK, false);
+      constexpr uint32_t id_o = idesc_bf16(128, DH, true);
+      for (int j = 0; j < T; ++j) {
+        const int st = j % STAGES;
+        if (!mbar_wait(&kv_full[st], (j / STAGES) & 1, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t kaddr = smem_u32(sKV + st * Sh::kStageBytes);
+        const uint32_t vaddr = kaddr + Sh::kTileBytes;
+        bool ok = true;
+        for (int t = 0; t < MT && ok; ++t) {
+          if (j > 0 && !mbar_wait(&s_free[t], (j - 1) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t qaddr = smem_u32(sQ + t * Sh::kRegions * 16384);
+#pragma unroll
+          for (int s = 0; s < DH / 16; ++s) {
+            const uint64_t ad = sdesc_sw128(qaddr + (s / 4) * 16384 + (s % 4) * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(kaddr + (s / 4) * 8192 + (s % 4) * 32, 16, 1024);
+            mma_bf16_ss(tmem + t * kNK, ad, bd, id_s, s > 0);
+          }
+          mma_commit(&s_full[t]);
+        }
+        for (int t = 0; t < MT && ok; ++t) {
+          if (!mbar_wait(&p_full[t], j & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t paddr = smem_u32(sP + t * 16384);
+#pragma unroll
+          for (int s = 0; s < kNK / 16; ++s) {
+            const uint64_t ad = sdesc_sw128(paddr + s * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(vaddr + s * 2048, 8192, 1024);
+            mma_bf16_ss(tmem + MT * kNK + t * DH, ad, bd, id_o, (j > 0 || s > 0));
+          }
+          mma_commit(&o_done[t]);
+        }
+        if (!ok) break;
+        mma_commit(&kv_empty[st]);
+      }
+    }
+  } else {
+    // ----------------------------------------------------------------- softmax
+    const int t = warp >> 2, qtr = warp & 3;
+    const int r = qtr * 32 + lane;
+    const int rho = (mg * MT + t) * 128 + r;
+    const bool row_ok = rho < rows_total;
+    const int i = row_ok ? rho / a.G : 0;
+    const int hh = row_ok ? rho % a.G : 0;
+    const uint32_t lane_base = static_cast<uint32_t>(qtr * 32) << 16;
+    const uint32_t tS = tmem + lane_base + t * kNK;
+    const uint32_t tO = tmem + lane_base + MT * kNK + t * DH;
+    unsigned char *prow = sP + t * 16384;
+    const uint64_t *mrow = a.mask + (static_cast<int64_t>(b) * n + i) * a.W;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < T; ++j) {
+      if (!warp_wait(&s_full[t], j & 1, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      // key validity: prefix positions below kv_len; tree nodes that are
+      // ancestors-or-self of this row's node
+      const bool prefix = j < np;
+      uint64_t keep;
+      if (prefix) {
+        const int valid = min(kNK, L - (p0 + j) * kNK);
+        keep = valid >= 64 ? ~0ull : ((1ull << valid) - 1ull);
+      } else {
+        keep = row_ok ? mrow[j - np] : 0ull;
+      }
+      // pass 1 over the S row in tensor memory: masked, scaled maximum
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float hv[32];
+        tmem_ld32(tS + 32 * half, hv);
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if ((keep >> (32 * half + c)) & 1ull) tmax = fmaxf(tmax, hv[c] * a.scale_log2);
+      }
+      const float m_new = fmaxf(m, tmax);
+      const float alpha = m_new > -INFINITY ? ex2_approx(m - m_new) : 1.f;
+      if (j > 0) {  // P of the previous tile has been consumed, O is final for it
+        if (!warp_wait(&o_done[t], (j - 1) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+      }
+      // pass 2: P = exp2(s - m_new) (bf16) into the 128B-swizzled K-major tile
+      float psum = 0.f;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float hv[32];
+        tmem_ld32(tS + 32 * half, hv);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const bool kp = ((keep >> (32 * half + c)) & 1ull) && m_new > -INFINITY;
+          hv[c] = kp ? ex2_approx(fmaf(hv[c], a.scale_log2, -m_new)) : 0.f;
+          psum += hv[c];
+        }
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8) {
+          __nv_bfloat162 h2[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) h2[e] = __floats2bfloat162_rn(hv[c8 * 8 + 2 * e], hv[c8 * 8 + 2 * e + 1]);
+          *reinterpret_cast<uint4 *>(prow + sw128_offset(r, half * 4 + c8)) = *reinterpret_cast<const uint4 *>(h2);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[t]);
+      l = l * alpha + psum;
+      m = m_new;
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int c0 = 0; c0 < DH; c0 += 32) {
+          float o[32];
+          tmem_ld32(tO + c0, o);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) o[c] *= alpha;
+          tmem_st32(tO + c0, o);
+        }
+      }
+      fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[t]);
+    }
+    if (ok && T > 0 && !warp_wait(&o_done[t], (T - 1) & 1, abort_flag)) ok = false;
+    tc_fence_after();
+    // tcgen05.ld is warp-collective (.sync.aligned): every lane executes it,
+    // rows past the last node only skip the global writes
+    const int h = g * a.G + hh;
+    const int64_t orow = (static_cast<int64_t>(b) * n + i) * a.Hq + h;
+    const int64_t prow_ = ((static_cast<int64_t>(b) * a.Hq + h) * a.S + split) * n + i;
+    const bool have = ok && T > 0;
+    const float inv = (have && l > 0.f) ? 1.f / l : 0.f;
+#pragma unroll
+    for (int c0 = 0; c0 < DH; c0 += 32) {
+      float o[32];
+      if (have) {
+        tmem_ld32(tO + c0, o);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) o[c] = 0.f;
+      }
+      if (!row_ok) continue;
+      if (a.S == 1) {
+        __nv_bfloat162 hv[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) hv[e] = __floats2bfloat162_rn(o[2 * e] * inv, o[2 * e + 1] * inv);
+        uint4 *dst = reinterpret_cast<uint4 *>(a.out + orow * DH + c0);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dst[e] = reinterpret_cast<const uint4 *>(hv)[e];
+      } else {
+        float4 *dst = reinterpret_cast<float4 *>(a.part_o + prow_ * DH + c0);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) dst[e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+      }
+    }
+    if (row_ok) {
+      if (a.S == 1) {
+        if (a.lse) a.lse[orow] = have ? (m + __log2f(l)) * kLn2 : -INFINITY;
+      } else {
+        a.part_ml[prow_ * 2 + 0] = have ? m * kLn2 : -INFINITY;
+        a.part_ml[prow_ * 2 + 1] = have ? l : 0.f;
+      }
+    }
+  }
+
+  // ---- teardown --------------------------------------------------------------
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (*abort_flag) {
+    if (tid == 0) report(a.status, EAGLE_ERR_TIMEOUT);
+    volatile int never = 0;
+    if (warp == mma_warp && lane == 0) {
+      // every MMA issued so far completes before tensor memory is released
+      mma_commit(teardown);
+      mbar_wait(teardown, 0, &never, 100000000ull);
+    }
+    if (warp == producer_warp && lane == 0) {
+      // copies still in flight complete before shared memory is released
+      for (int j = max(0, issued - STAGES); j < issued; ++j)
+        mbar_wait(&kv_full[j % STAGES], (j / STAGES) & 1, &never, 100000000ull);
+    }
+    __syncthreads();
+  }
+  if (warp == mma_warp) tmem_dealloc(tmem, Sh::kTmemCols);
+}
+
+// ---- host side ---------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2D bf16 tensor [rows, dh] viewed in 64 x 64 boxes with 128-byte swizzle.
+static bool make_kv_map(CUtensorMap *map, const void *base, int64_t rows, int dh) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(dh), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(dh) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kNK)};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct TcPlan {
+  int MT, mgroups, S, stages;
+};
+
+static TcPlan tc_plan(int B, int n, int Hq, int Hkv, int dh, int Lmax, int num_sms) {
+  TcPlan p;
+  const int G = Hq / Hkv;
+  const int tiles = (n * G + 127) / 128;
+  p.MT = tiles <= 1 ? 1 : (tiles <= 2 || dh == 128) ? 2 : 4;
+  p.mgroups = (tiles + p.MT - 1) / p.MT;
+  p.stages = 4;
+  const int64_t base = static_cast<int64_t>(B) * Hkv * p.mgroups;
+  const int ctas_per_sm = (dh == 64 && p.MT == 1) ? 2 : 1;
+  const int64_t slots = static_cast<int64_t>(num_sms) * ctas_per_sm;
+  int64_t S = base >= slots ? 1 : (slots + base - 1) / base;
+  const int64_t ptiles = (Lmax + kNK - 1) / kNK;
+  if (S > ptiles / 2) S = ptiles / 2;
+  if (S > 32) S = 32;
+  if (S < 1) S = 1;
+  p.S = static_cast<int>(S);
+  return p;
+}
+
+size_t attn_tc_workspace_bytes(int B, int n, int Hq, int Hkv, int dh, int Lmax, int num_sms) {
+  const TcPlan p = tc_plan(B, n, Hq, Hkv, dh, Lmax, num_sms);
+  if (p.S == 1) return 0;
+  return sizeof(float) * static_cast<size_t>(B) * Hq * p.S * n * (dh + 2);
+}
+
+cudaError_t launch_attn_combine_bf16(const float *part_o, const float *part_ml, int B, int n, int Hq, int dh,
+                                     int S, void *out, float *lse, cudaStream_t st);
+
+template <int DH, int MT>
+static cudaError_t launch_tc_t(const CUtensorMap *maps, const TcArgs &a, const TcPlan &p, cudaStream_t st) {
+  constexpr int STAGES = 4;
+  using Sh = TcShape<DH, MT, STAGES>;
+  static_assert(Sh::kSmem <= 232448, "shared memory budget");
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(tree_attn_tc_kernel<DH, MT, STAGES>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  dim3 grid(p.S, p.mgroups, a.B * a.Hkv);
+  tree_attn_tc_kernel<DH, MT, STAGES><<<grid, Sh::kThreads, Sh::kSmem, st>>>(maps[0], maps[1], maps[2], maps[3], a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tree_attn_tc(const void *q, const void *k_cache, const void *v_cache, const int32_t *kv_len,
+                                const void *k_tree, const void *v_tree, const uint64_t *mask, int B, int n,
+                                int Hq, int Hkv, int dh, int Lmax, float scale, void *out, float *lse, void *ws,
+                                int32_t *status, int num_sms, cudaStream_t st) {
+  const TcPlan p = tc_plan(B, n, Hq, Hkv, dh, Lmax, num_sms);
+  CUtensorMap maps[4];
+  const int64_t cache_rows = static_cast<int64_t>(B) * Hkv * Lmax;
+  const int64_t tree_rows = static_cast<int64_t>(B) * Hkv * n;
+  if (!make_kv_map(&maps[0], k_cache, cache_rows > 0 ? cache_rows : 1, dh) ||
+      !make_kv_map(&maps[1], v_cache, cache_rows > 0 ? cache_rows : 1, dh) ||
+      !make_kv_map(&maps[2], k_tree, tree_rows, dh) || !make_kv_map(&maps[3], v_tree, tree_rows, dh))
+    return cudaErrorInvalidValue;
+  TcArgs a;
+  a.q = reinterpret_cast<const __nv_bfloat16 *>(q);
+  a.k_cache = reinterpret_cast<const __nv_bfloat16 *>(k_cache);
+  a.v_cache = reinterpret_cast<const __nv_bfloat16 *>(v_cache);
+  a.kv_len = kv_len;
+  a.mask = mask;
+  a.B = B; a.n = n; a.Hq = Hq; a.Hkv = Hkv; a.G = Hq / Hkv; a.Lmax = Lmax; a.S = p.S;
+  a.W = (n + 63) / 64;
+  a.scale_log2 = scale * kLog2e;
+  a.out = reinterpret_cast<__nv_bfloat16 *>(out);
+  a.lse = lse;
+  a.part_o = reinterpret_cast<float *>(ws);
+  a.part_ml = a.part_o + static_cast<size_t>(B) * Hq * p.S * n * dh;
+  a.status = status;
+  cudaError_t e;
+  if (dh == 64) {
+    e = p.MT == 1 ? launch_tc_t<64, 1>(maps, a, p, st)
+                  : p.MT == 2 ? launch_tc_t<64, 2>(maps, a, p, st) : launch_tc_t<64, 4>(maps, a, p, st);
+  } else {
+    e = p.MT == 1 ? launch_tc_t<128, 1>(maps, a, p, st) : launch_tc_t<128, 2>(maps, a, p, st);
+  }
+  if (e != cudaSuccess || p.S == 1) return e;
+  return launch_attn_combine_bf16(a.part_o, a.part_ml, B, n, Hq, dh, p.S, out, lse, st);
+}
+
+}  // namespace eagle

@@ -51,7 +51,7 @@ class TreeStep:
         if self.attn_out is None or self.attn_out.shape != q.shape or self.attn_out.dtype != q.dtype:
             self.attn_out = torch.empty_like(q)
         tree_attn(q, k_cache, v_cache, kv_len, k_tree, v_tree, self.tree["mask"], scale,
-                  self.attn_out, self.lse, self.ws_attn)
+                  self.attn_out, self.lse, self.ws_attn, self.status)
 
     def verify(self, target, uniforms=None):
         verify(target, self.tree["tok"], self.tree["parent"], self.D, self.mode, self.temperature,
