@@ -101,6 +101,30 @@ int eagle_draft_topk(const void *logits, int dtype, int B, int D, int k, int V,
                      eagle_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Stage 1 without caller scratch: eagle_draft_topk_noalloc.
+ * The paper has no counterpart to this entry point; it exists for callers
+ * that cannot give the library scratch memory — plugins or custom-op hooks
+ * of a host runtime that hands over only input and output buffers and owns
+ * all device memory, or processes whose device-memory budget is fixed up
+ * front.  Same arguments and results as eagle_draft_topk, without the
+ * workspace.  It allocates nothing: its scratch is a fixed array of
+ * EAGLE_NOALLOC_SCRATCH_BYTES compiled into the library, present on every GPU
+ * that loads the library until the process exits.  The array's device
+ * address is looked up on the first call made while a device is current.
+ * Sizes whose scratch would exceed the array return EAGLE_ERR_WORKSPACE
+ * (eagle_draft_topk_workspace_size gives the need).  Every call on a device
+ * shares the one array, so calls that may overlap on the GPU (different
+ * streams or host threads) race and must be serialised by the caller; each
+ * call clears the part of the array that must start at zero.
+ * ------------------------------------------------------------------------ */
+#define EAGLE_NOALLOC_SCRATCH_BYTES (1u << 17) /* 128 KiB */
+
+int eagle_draft_topk_noalloc(const void *logits, int dtype, int B, int D, int k,
+                             int V, int64_t ld, int32_t *tok, float *conf,
+                             float *stats, int32_t *status,
+                             eagle_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Stage 2 — dynamic draft tree.
  * [EAGLE-2] section "動的ドラフトツリーの構築アルゴリズム": V_i = product of
  * the confidences on the root path (V_i equation); at every depth the k

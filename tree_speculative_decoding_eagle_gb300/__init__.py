@@ -25,7 +25,7 @@ GREEDY, SAMPLE = 0, 1
 
 EXPORTED = (
     "eagle_status_string", "eagle_version",
-    "eagle_draft_topk_workspace_size", "eagle_draft_topk",
+    "eagle_draft_topk_workspace_size", "eagle_draft_topk", "eagle_draft_topk_noalloc",
     "eagle_tree_build", "eagle_tree_mask",
     "eagle_tree_attn_workspace_size", "eagle_tree_attn",
     "eagle_verify_workspace_size", "eagle_verify",
@@ -52,6 +52,7 @@ def load_library(path=LIB_PATH):
         "eagle_version": (I, []),
         "eagle_draft_topk_workspace_size": (SZ, [I, I, I, I]),
         "eagle_draft_topk": (I, [P, I, I, I, I, I, I64, P, P, P, P, P, SZ, P]),
+        "eagle_draft_topk_noalloc": (I, [P, I, I, I, I, I, I64, P, P, P, P, P]),
         "eagle_tree_build": (I, [P, P, I, I, I, I, P, P, P, P, P, P, P, P, P, P]),
         "eagle_tree_mask": (I, [P, I, I, P, P]),
         "eagle_tree_attn_workspace_size": (SZ, [I, I, I, I, I, I, I]),
@@ -132,6 +133,27 @@ def draft_topk(logits, k, tok=None, conf=None, stats=None, workspace=None, statu
                                 _ptr(conf), _ptr(stats), _ptr(status), _ptr(wbuf), wbytes,
                                 _stream(stream)),
            "eagle_draft_topk")
+    return tok, conf, stats
+
+
+def draft_topk_noalloc(logits, k, tok=None, conf=None, stats=None, status=None, stream=None):
+    """draft_topk for callers that cannot provide scratch memory: the library
+    uses its own fixed scratch array (calls that overlap on the GPU race)."""
+    lib = load_library()
+    _cuda(logits, "logits")
+    B, D, kk, V = logits.shape
+    if kk != k or logits.stride(-1) != 1:
+        raise EagleError("logits must be [B, D, k, V] with unit stride in V")
+    ld = logits.stride(2)
+    if logits.stride(1) != k * ld or logits.stride(0) != D * k * ld:
+        raise EagleError("logits rows must be evenly spaced")
+    dev = logits.device
+    tok = tok if tok is not None else torch.empty((B, D, k, k), dtype=torch.int32, device=dev)
+    conf = conf if conf is not None else torch.empty((B, D, k, k), dtype=torch.float32, device=dev)
+    stats = stats if stats is not None else torch.empty((B, D, k, 2), dtype=torch.float32, device=dev)
+    _check(lib.eagle_draft_topk_noalloc(_ptr(logits), _dtype_code(logits), B, D, k, V, ld, _ptr(tok),
+                                        _ptr(conf), _ptr(stats), _ptr(status), _stream(stream)),
+           "eagle_draft_topk_noalloc")
     return tok, conf, stats
 
 
