@@ -60,7 +60,7 @@ struct TcShape {
 };
 
 template <int DH, int MT, int STAGES>
-__global__ void __launch_bounds__(MT * 128 + 64, 1)
+__global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
     tree_attn_tc_kernel(const __grid_constant__ CUtensorMap kc_map, const __grid_constant__ CUtensorMap vc_map,
                         const __grid_constant__ CUtensorMap kt_map, const __grid_constant__ CUtensorMap vt_map,
                         TcArgs a) {
@@ -192,15 +192,15 @@ __global__ void __launch_bounds__(MT * 128 + 64, 1)
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(128, kNK, false);
       constexpr uint32_t id_o = idesc_bf16(128, DH, true);
-      for (int j = 0; j < T; ++j) {
+      // S for tile j+1 is issued as soon as the softmax has read tile j's S,
+      // so it overlaps that softmax; P.V for tile j follows its P.
+      auto issue_s = [&](int j) -> bool {
         const int st = j % STAGES;
-        if (!mbar_wait(&kv_full[st], (j / STAGES) & 1, abort_flag)) break;
+        if (!mbar_wait(&kv_full[st], (j / STAGES) & 1, abort_flag)) return false;
         tc_fence_after();
         const uint32_t kaddr = smem_u32(sKV + st * Sh::kStageBytes);
-        const uint32_t vaddr = kaddr + Sh::kTileBytes;
-        bool ok = true;
-        for (int t = 0; t < MT && ok; ++t) {
-          if (j > 0 && !mbar_wait(&s_free[t], (j - 1) & 1, abort_flag)) { ok = false; break; }
+        for (int t = 0; t < MT; ++t) {
+          if (j > 0 && !mbar_wait(&s_free[t], (j - 1) & 1, abort_flag)) return false;
           tc_fence_after();
           const uint32_t qaddr = smem_u32(sQ + t * Sh::kRegions * 16384);
 #pragma unroll
@@ -211,6 +211,13 @@ __global__ void __launch_bounds__(MT * 128 + 64, 1)
           }
           mma_commit(&s_full[t]);
         }
+        return true;
+      };
+      bool ok = T == 0 || issue_s(0);
+      for (int j = 0; j < T && ok; ++j) {
+        const int st = j % STAGES;
+        if (j + 1 < T && !issue_s(j + 1)) break;
+        const uint32_t vaddr = smem_u32(sKV + st * Sh::kStageBytes) + Sh::kTileBytes;
         for (int t = 0; t < MT && ok; ++t) {
           if (!mbar_wait(&p_full[t], j & 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
@@ -223,8 +230,7 @@ __global__ void __launch_bounds__(MT * 128 + 64, 1)
           }
           mma_commit(&o_done[t]);
         }
-        if (!ok) break;
-        mma_commit(&kv_empty[st]);
+        if (ok) mma_commit(&kv_empty[st]);
       }
     }
   } else {
@@ -240,11 +246,19 @@ __global__ void __launch_bounds__(MT * 128 + 64, 1)
     const uint32_t tO = tmem + lane_base + MT * kNK + t * DH;
     unsigned char *prow = sP + t * 16384;
     const uint64_t *mrow = a.mask + (static_cast<int64_t>(b) * n + i) * a.W;
+    // m is the exponent base of this row's P and O (scaled, base-2 units).  It
+    // is raised only when the row maximum exceeds it by more than 8, so P
+    // stays below 2^8 and O is rescaled rarely.
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < T; ++j) {
       if (!warp_wait(&s_full[t], j & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
+      float sv[kNK];
+      tmem_ld64(tS, sv);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[t]);  // S stays in registers
       // key validity: prefix positions below kv_len; tree nodes that are
       // ancestors-or-self of this row's node
       const bool prefix = j < np;
@@ -255,48 +269,48 @@ __global__ void __launch_bounds__(MT * 128 + 64, 1)
       } else {
         keep = row_ok ? mrow[j - np] : 0ull;
       }
-      // pass 1 over the S row in tensor memory: masked, scaled maximum
-      float tmax = -INFINITY;
+      const bool dense = __all_sync(0xffffffffu, keep == ~0ull);
+      if (!dense) {
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float hv[32];
-        tmem_ld32(tS + 32 * half, hv);
-#pragma unroll
-        for (int c = 0; c < 32; ++c)
-          if ((keep >> (32 * half + c)) & 1ull) tmax = fmaxf(tmax, hv[c] * a.scale_log2);
+        for (int c = 0; c < kNK; ++c) sv[c] = ((keep >> c) & 1ull) ? sv[c] : -INFINITY;
       }
-      const float m_new = fmaxf(m, tmax);
-      const float alpha = m_new > -INFINITY ? ex2_approx(m - m_new) : 1.f;
+      float mx[4] = {sv[0], sv[1], sv[2], sv[3]};
+#pragma unroll
+      for (int c = 4; c < kNK; c += 8) {
+        mx[0] = fmax3(mx[0], sv[c], sv[c + 4]);
+        mx[1] = fmax3(mx[1], sv[c + 1], sv[c + 5]);
+        mx[2] = fmax3(mx[2], sv[c + 2], sv[c + 6]);
+        mx[3] = fmax3(mx[3], sv[c + 3], sv[c + 7]);
+      }
+      const float tmax = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]) * a.scale_log2;  // scale > 0
+      const bool raise = tmax > m + 8.f;
+      const float base = raise ? tmax : m;
+      const float alpha = raise ? ex2_approx(m - tmax) : 1.f;  // m = -inf gives 0
+      m = base;
       if (j > 0) {  // P of the previous tile has been consumed, O is final for it
         if (!warp_wait(&o_done[t], (j - 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
       }
-      // pass 2: P = exp2(s - m_new) (bf16) into the 128B-swizzled K-major tile
-      float psum = 0.f;
+      // P = exp2(s*scale - base) as bf16 into the 128B-swizzled K-major tile
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+      // a row with no valid key yet has base -inf and only -inf scores: any
+      // finite exponent base then gives 0
+      const float nb = base > -INFINITY ? -base : 0.f;
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float hv[32];
-        tmem_ld32(tS + 32 * half, hv);
+      for (int c8 = 0; c8 < kNK / 8; ++c8) {
+        float pv[8];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const bool kp = ((keep >> (32 * half + c)) & 1ull) && m_new > -INFINITY;
-          hv[c] = kp ? ex2_approx(fmaf(hv[c], a.scale_log2, -m_new)) : 0.f;
-          psum += hv[c];
+        for (int e = 0; e < 8; ++e) {
+          pv[e] = ex2_approx(fmaf(sv[c8 * 8 + e], a.scale_log2, nb));  // -inf gives 0
+          ps[e & 3] += pv[e];
         }
+        __nv_bfloat162 h2[4];
 #pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
-          __nv_bfloat162 h2[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) h2[e] = __floats2bfloat162_rn(hv[c8 * 8 + 2 * e], hv[c8 * 8 + 2 * e + 1]);
-          *reinterpret_cast<uint4 *>(prow + sw128_offset(r, half * 4 + c8)) = *reinterpret_cast<const uint4 *>(h2);
-        }
+        for (int e = 0; e < 4; ++e) h2[e] = __floats2bfloat162_rn(pv[2 * e], pv[2 * e + 1]);
+        *reinterpret_cast<uint4 *>(prow + sw128_offset(r, c8)) = *reinterpret_cast<const uint4 *>(h2);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[t]);
-      l = l * alpha + psum;
-      m = m_new;
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+      l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+      if (j > 0 && __any_sync(0xffffffffu, raise)) {
 #pragma unroll
         for (int c0 = 0; c0 < DH; c0 += 32) {
           float o[32];
@@ -412,6 +426,9 @@ struct TcPlan {
   int MT, mgroups, S, stages;
 };
 
+// Launch plan: M-tiles per CTA, and the KV split S chosen to minimise
+// (waves of CTAs) x (key tiles per CTA + the extra traffic a split's partial
+// results cost, in key-tile units).
 static TcPlan tc_plan(int B, int n, int Hq, int Hkv, int dh, int Lmax, int num_sms) {
   TcPlan p;
   const int G = Hq / Hkv;
@@ -420,14 +437,22 @@ static TcPlan tc_plan(int B, int n, int Hq, int Hkv, int dh, int Lmax, int num_s
   p.mgroups = (tiles + p.MT - 1) / p.MT;
   p.stages = 4;
   const int64_t base = static_cast<int64_t>(B) * Hkv * p.mgroups;
-  const int ctas_per_sm = (dh == 64 && p.MT == 1) ? 2 : 1;
+  const int ctas_per_sm = p.MT == 1 ? 2 : 1;
   const int64_t slots = static_cast<int64_t>(num_sms) * ctas_per_sm;
-  int64_t S = base >= slots ? 1 : (slots + base - 1) / base;
   const int64_t ptiles = (Lmax + kNK - 1) / kNK;
-  if (S > ptiles / 2) S = ptiles / 2;
-  if (S > 32) S = 32;
-  if (S < 1) S = 1;
-  p.S = static_cast<int>(S);
+  const double split_cost = static_cast<double>(G) * n / 32.0 / p.mgroups;
+  int best = 1;
+  double best_cost = 1e30;
+  for (int S = 1; S <= 32 && S <= ptiles; ++S) {
+    const int64_t waves = (base * S + slots - 1) / slots;
+    const double per_cta = static_cast<double>((ptiles + S - 1) / S) + (S > 1 ? split_cost : 0.0);
+    const double cost = waves * per_cta;
+    if (cost < best_cost * 0.97) {  // prefer fewer splits unless clearly better
+      best_cost = cost;
+      best = S;
+    }
+  }
+  p.S = best;
   return p;
 }
 
@@ -440,9 +465,16 @@ size_t attn_tc_workspace_bytes(int B, int n, int Hq, int Hkv, int dh, int Lmax, 
 cudaError_t launch_attn_combine_bf16(const float *part_o, const float *part_ml, int B, int n, int Hq, int dh,
                                      int S, void *out, float *lse, cudaStream_t st);
 
+// Stages of the K/V ring: single-tile dh=128 CTAs keep two stages so that two
+// CTAs fit in one SM's shared memory.
+template <int DH, int MT>
+constexpr int tc_stages() { return (DH == 128 && MT == 1) ? 2 : 4; }
+template <int DH, int MT>
+constexpr int tc_ctas_per_sm() { return MT == 1 ? 2 : 1; }
+
 template <int DH, int MT>
 static cudaError_t launch_tc_t(const CUtensorMap *maps, const TcArgs &a, const TcPlan &p, cudaStream_t st) {
-  constexpr int STAGES = 4;
+  constexpr int STAGES = tc_stages<DH, MT>();
   using Sh = TcShape<DH, MT, STAGES>;
   static_assert(Sh::kSmem <= 232448, "shared memory budget");
   static bool configured = false;
