@@ -13,9 +13,9 @@
 // lane maximum of a warp (a 32-lane bitonic sort per chunk) bounds the top k
 // from below, and the block keeps the largest such bound.  Values at or
 // above the bound are appended to a per-warp shared-memory buffer by a
-// ballot scan, so only about k candidates per warp survive; the buffer is
-// merged into the warp's top-K list (register insertion plus bitonic
-// shuffles) when full and at the end.  Warp lists
+// ballot scan, so only about k candidates per warp survive.  Merges keep the
+// code small: the k best of a set of unique keys are found by counting, for
+// each key, how many keys are larger (its rank), in shared memory.  Warp lists
 // merge block-wide through shared memory.  With S > 1 the last CTA of a row
 // to finish (atomic ticket in the workspace) merges the S partial results;
 // no CTA ever waits for another.
@@ -41,42 +41,13 @@ constexpr int kDraftChunkVec = kDraftThreads * kDraftUnroll;   // 16-byte vector
 constexpr int kDraftStages = 4;                                // chunks in flight per CTA
 constexpr int kDraftSmem = kDraftStages * kDraftChunkVec * 16 + 128;
 
-template <int K>
-struct alignas(16) DraftPartial {
-  float m, s;
-  uint32_t pad[2];
-  uint64_t keys[K];
-};
-
+// Workspace: [tickets: u32 per row][(max, sum) per row and split][k keys per
+// row and split], each part 256-byte aligned.
 __host__ __device__ inline size_t draft_counter_bytes(int B, int R) {
   return (static_cast<size_t>(B) * R * sizeof(uint32_t) + 255) / 256 * 256;
 }
-
-// Write the k best keys of a finished row (all lanes of the calling warp hold
-// the same descending list).
-template <int K>
-__device__ __forceinline__ void draft_finalize(const DraftArgs &a, int b, int d, int j,
-                                               const uint64_t (&list)[K], float M, float Z) {
-  const int lane = threadIdx.x & 31;
-  const int64_t slot = ((static_cast<int64_t>(b) * a.D + d) * a.k + j);
-  if (lane < a.k) {
-    uint64_t key = 0;
-#pragma unroll
-    for (int q = 0; q < K; ++q)
-      if (q == lane) key = list[q];
-    int32_t t = -1;
-    float c = 0.f;
-    if (key) {
-      t = static_cast<int32_t>(key_token(key));
-      c = expf(key_value(key) - M) / Z;
-    }
-    a.tok[slot * a.k + lane] = t;
-    a.conf[slot * a.k + lane] = c;
-  }
-  if (lane == 0 && a.stats) {
-    a.stats[slot * 2 + 0] = M;
-    a.stats[slot * 2 + 1] = logf(Z);
-  }
+__host__ __device__ inline size_t draft_ms_bytes(int B, int R, int S) {
+  return (static_cast<size_t>(B) * R * S * sizeof(float2) + 255) / 256 * 256;
 }
 
 // Bitonic sort of one float per lane across the warp, descending by lane.
@@ -94,34 +65,56 @@ __device__ __forceinline__ float warp_sort_desc(float x, int lane) {
   return x;
 }
 
-// Merge the warp's candidate buffer into the warp list (held identically by
-// every lane); afterwards every lane again holds the warp's top K.
-template <int K>
-__device__ __forceinline__ void draft_flush(uint64_t (&list)[K], const uint64_t *buf, int fill,
-                                            int lane) {
+// Rank of `key` among set[0..n): the number of larger keys (keys are unique).
+__device__ __forceinline__ int rank_in(uint64_t key, const uint64_t *set, int n) {
+  int r = 0;
+  for (int q = 0; q < n; ++q) r += set[q] > key;
+  return r;
+}
+
+// The warp's k best of its list wl[0..*wn) and its buffer buf[0..fill),
+// written back to wl in descending order (whole warp, rank by counting).
+__device__ __forceinline__ void warp_compact(uint64_t *wl, int *wn, uint64_t *buf, int fill, uint64_t *tmp,
+                                             int k, int lane) {
   __syncwarp();
-  if (lane != 0) {
-#pragma unroll
-    for (int q = 0; q < K; ++q) list[q] = 0;
+  const int n0 = *wn;
+  const int C = n0 + fill;
+  for (int i = lane; i < C; i += 32) {
+    const uint64_t key = i < n0 ? wl[i] : buf[i - n0];
+    const int r = rank_in(key, wl, n0) + rank_in(key, buf, fill);
+    if (r < k) tmp[r] = key;
   }
-  for (int i = lane; i < fill; i += 32) list_insert<K>(list, buf[i]);
-  warp_topk<K>(list);
+  __syncwarp();
+  const int nk = C < k ? C : k;
+  if (lane < nk) wl[lane] = tmp[lane];
+  if (lane == 0) *wn = nk;
   __syncwarp();
 }
 
-template <typename T, int K>
+template <typename T>
 __global__ void __launch_bounds__(kDraftThreads) draft_topk_kernel(DraftArgs a) {
   using VT = VecTraits<T>;
   constexpr int VEC = VT::kElems;
-  constexpr int BUF = 32 * VEC;  // one full vector step of the warp always fits
-  __shared__ uint64_t s_buf[kDraftThreads / 32][2 * BUF];
+  constexpr int CAP = 64 * VEC;  // candidate buffer per warp (two full vector steps)
+  constexpr int NW = kDraftThreads / 32;
+  __shared__ uint64_t s_buf[NW][CAP];
+  __shared__ uint64_t s_wl[NW][32], s_tmp[NW][32];
+  __shared__ int s_wn[NW];
+  __shared__ uint64_t s_top[32];
+  __shared__ float s_m[NW], s_s[NW];
+  __shared__ int s_last;
+  __shared__ volatile int s_abort;
+  __shared__ unsigned s_thr;  // block prune bound (order-preserving bits)
+
   const int s = blockIdx.x;
   const int rg = blockIdx.y;  // b * R + r
   const int b = rg / a.R, r = rg % a.R;
   const int d = r == 0 ? 0 : 1 + (r - 1) / a.k;
   const int j = r == 0 ? 0 : (r - 1) % a.k;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int k = a.k;
   uint64_t *buf = s_buf[warp];
+  uint64_t *wl = s_wl[warp];
 
   const T *row = reinterpret_cast<const T *>(a.logits) +
                  ((static_cast<int64_t>(b) * a.D + d) * a.k + j) * a.ld;
@@ -134,14 +127,13 @@ __global__ void __launch_bounds__(kDraftThreads) draft_topk_kernel(DraftArgs a) 
   extern __shared__ __align__(128) unsigned char dsm[];
   uint4 *stage_buf = reinterpret_cast<uint4 *>(dsm);
   uint64_t *full = reinterpret_cast<uint64_t *>(dsm + kDraftStages * kDraftChunkVec * 16);
-  __shared__ volatile int s_abort;
-  __shared__ unsigned s_thr;  // block prune bound (order-preserving bits)
   if (tid == 0) {
     s_abort = 0;
     s_thr = ordered_u32(-INFINITY);
     for (int q = 0; q < kDraftStages; ++q) sm100::mbar_init(&full[q], 1);
     sm100::mbar_init_fence();
   }
+  if (lane == 0) s_wn[warp] = 0;
   __syncthreads();
   auto issue = [&](int c) {
     const int64_t first = v0 + static_cast<int64_t>(c) * kDraftChunkVec;
@@ -154,9 +146,6 @@ __global__ void __launch_bounds__(kDraftThreads) draft_topk_kernel(DraftArgs a) 
     for (int c = 0; c < min(kDraftStages, n_chunks); ++c) issue(c);
 
   float m = -INFINITY, sum = 0.f;
-  uint64_t list[K];  // the warp's top K so far, identical in every lane
-#pragma unroll
-  for (int q = 0; q < K; ++q) list[q] = 0;
   float lmax = -INFINITY;  // this lane's largest value so far
   float thr = -INFINITY;   // prune bound: at least k values of the slice are >= thr
   int fill = 0;            // candidates waiting in the warp buffer
@@ -202,10 +191,12 @@ __global__ void __launch_bounds__(kDraftThreads) draft_topk_kernel(DraftArgs a) 
     }
     // Lane maxima are distinct elements, so the k-th largest of the warp's
     // lane maxima has at least k elements at or above it; so has any other
-    // warp's bound, and the block keeps the largest of them.
+    // warp's bound and the k-th key of a full warp list.  The block keeps the
+    // largest bound.
     {
-      float y = warp_sort_desc(lmax, lane);
-      const float tw = __shfl_sync(0xffffffffu, y, a.k - 1);
+      const float y = warp_sort_desc(lmax, lane);
+      float tw = __shfl_sync(0xffffffffu, y, k - 1);
+      if (s_wn[warp] == k) tw = fmaxf(tw, key_value(wl[k - 1]));
       if (tw > -INFINITY) atomicMax(&s_thr, ordered_u32(tw));
       thr = fmaxf(thr, fmaxf(tw, from_ordered_u32(s_thr)));
     }
@@ -230,8 +221,8 @@ __global__ void __launch_bounds__(kDraftThreads) draft_topk_kernel(DraftArgs a) 
           if (lane >= o) incl += v;
         }
         const int total = __shfl_sync(0xffffffffu, incl, 31);
-        if (fill + total > 2 * BUF) {
-          draft_flush<K>(list, buf, fill, lane);
+        if (fill + total > CAP) {
+          warp_compact(wl, &s_wn[warp], buf, fill, s_tmp[warp], k, lane);
           fill = 0;
         }
         if (cm) {
@@ -258,89 +249,106 @@ __global__ void __launch_bounds__(kDraftThreads) draft_topk_kernel(DraftArgs a) 
     }
     return;
   }
-  if (fill > 0) draft_flush<K>(list, buf, fill, lane);
+  if (fill > 0) warp_compact(wl, &s_wn[warp], buf, fill, s_tmp[warp], k, lane);
 
-  // ---- warp statistics ------------------------------------------------------
+  // ---- block: softmax statistics and the top k of the warp lists ------------
   {
     float mw = warp_max(m);
     float sw = (m == -INFINITY) ? 0.f : sum * ex2_approx((m - mw) * kLog2e);
     sw = warp_sum(sw);
-    m = mw;
-    sum = sw;
-  }
-  __shared__ uint64_t s_keys[kDraftThreads / 32][K];
-  __shared__ float s_m[kDraftThreads / 32], s_s[kDraftThreads / 32];
-  __shared__ int s_last;
-  if (lane == 0) {
-    s_m[warp] = m;
-    s_s[warp] = sum;
-  }
-  if (lane < K) {
-#pragma unroll
-    for (int q = 0; q < K; ++q)
-      if (q == lane) s_keys[warp][q] = list[q];
+    if (lane == 0) {
+      s_m[warp] = mw;
+      s_s[warp] = sw;
+    }
   }
   __syncthreads();
-  if (warp != 0) return;
-
-  // ---- block merge (warp 0) -------------------------------------------------
-  constexpr int NW = kDraftThreads / 32;
-#pragma unroll
-  for (int q = 0; q < K; ++q) list[q] = lane < NW ? s_keys[lane][q] : 0ull;
-  warp_topk<K>(list);  // every lane ends with the block's top K
+  // gather the warp lists into one array (the first warp's buffer)
+  uint64_t *U = s_buf[0];
+  int C = 0;
+  for (int w = 0; w < NW; ++w) {
+    const int nw = s_wn[w];
+    if (tid < nw) U[C + tid] = s_wl[w][tid];
+    C += nw;
+  }
+  if (tid < 32) s_top[tid] = 0ull;
+  __syncthreads();
+  for (int i = tid; i < C; i += kDraftThreads) {
+    const uint64_t key = U[i];
+    const int rk = rank_in(key, U, C);
+    if (rk < k) s_top[rk] = key;
+  }
   float M = s_m[0], Z = s_s[0];
   for (int w = 1; w < NW; ++w) lse_combine(M, Z, s_m[w], s_s[w]);
+  __syncthreads();
 
+  const int64_t slot = ((static_cast<int64_t>(b) * a.D + d) * a.k + j);
+  auto finalize = [&](const uint64_t *top, float Mf, float Zf) {
+    if (tid < k) {
+      const uint64_t key = top[tid];
+      int32_t t = -1;
+      float cf = 0.f;
+      if (key) {
+        t = static_cast<int32_t>(key_token(key));
+        cf = expf(key_value(key) - Mf) / Zf;
+      }
+      a.tok[slot * a.k + tid] = t;
+      a.conf[slot * a.k + tid] = cf;
+    }
+    if (tid == 0 && a.stats) {
+      a.stats[slot * 2 + 0] = Mf;
+      a.stats[slot * 2 + 1] = logf(Zf);
+    }
+  };
   if (a.S == 1) {
-    draft_finalize<K>(a, b, d, j, list, M, Z);
+    finalize(s_top, M, Z);
     return;
   }
 
   // ---- split rows: publish the partial, the last CTA merges ---------------
   uint32_t *counters = reinterpret_cast<uint32_t *>(a.ws);
-  DraftPartial<K> *parts = reinterpret_cast<DraftPartial<K> *>(a.ws + draft_counter_bytes(a.B, a.R));
-  DraftPartial<K> *mine = parts + static_cast<int64_t>(rg) * a.S + s;
-  if (lane < K) {
-#pragma unroll
-    for (int q = 0; q < K; ++q)
-      if (q == lane) mine->keys[q] = list[q];
-  }
-  if (lane == 0) {
-    mine->m = M;
-    mine->s = Z;
-  }
+  float2 *parts_ms = reinterpret_cast<float2 *>(a.ws + draft_counter_bytes(a.B, a.R));
+  uint64_t *parts_keys =
+      reinterpret_cast<uint64_t *>(a.ws + draft_counter_bytes(a.B, a.R) + draft_ms_bytes(a.B, a.R, a.S));
+  const int64_t prow = static_cast<int64_t>(rg) * a.S;
+  if (tid < k) parts_keys[(prow + s) * k + tid] = s_top[tid];
+  if (tid == 0) parts_ms[prow + s] = make_float2(M, Z);
   __threadfence();
-  __syncwarp();
-  if (lane == 0) s_last = (atomicAdd(counters + rg, 1u) == static_cast<uint32_t>(a.S - 1));
-  __syncwarp();
+  __syncthreads();
+  if (tid == 0) s_last = (atomicAdd(counters + rg, 1u) == static_cast<uint32_t>(a.S - 1));
+  __syncthreads();
   if (!s_last) return;
   __threadfence();
 
-  const DraftPartial<K> *row_parts = parts + static_cast<int64_t>(rg) * a.S;
-  float pm = -INFINITY, ps = 0.f;
-  if (lane < a.S) {
-#pragma unroll
-    for (int q = 0; q < K; ++q) list[q] = __ldcg(reinterpret_cast<const unsigned long long *>(&row_parts[lane].keys[q]));
-    pm = __ldcg(&row_parts[lane].m);
-    ps = __ldcg(&row_parts[lane].s);
-  } else {
-#pragma unroll
-    for (int q = 0; q < K; ++q) list[q] = 0;
+  const int CS = a.S * k;
+  for (int i = tid; i < CS; i += kDraftThreads)
+    U[i] = __ldcg(reinterpret_cast<const unsigned long long *>(parts_keys + prow * k + i));
+  if (tid < 32) s_top[tid] = 0ull;
+  __syncthreads();
+  for (int i = tid; i < CS; i += kDraftThreads) {
+    const uint64_t key = U[i];
+    if (!key) continue;  // a slice with fewer than k finite values
+    const int rk = rank_in(key, U, CS);
+    if (rk < k) s_top[rk] = key;
   }
-  warp_topk<K>(list);
-  M = warp_max(pm);
-  Z = warp_sum(pm == -INFINITY ? 0.f : ps * ex2_approx((pm - M) * kLog2e));
-  draft_finalize<K>(a, b, d, j, list, M, Z);
-  if (lane == 0) counters[rg] = 0;  // leave the ticket zeroed for the next call
+  if (warp == 0) {
+    float pm = -INFINITY, ps = 0.f;
+    for (int q = lane; q < a.S; q += 32) {
+      const float2 ms = __ldcg(parts_ms + prow + q);
+      lse_combine(pm, ps, ms.x, ms.y);
+    }
+    const float Mw = warp_max(pm);
+    const float Zw = warp_sum(pm == -INFINITY ? 0.f : ps * ex2_approx((pm - Mw) * kLog2e));
+    if (lane == 0) {
+      s_m[0] = Mw;
+      s_s[0] = Zw;
+    }
+  }
+  __syncthreads();
+  finalize(s_top, s_m[0], s_s[0]);
+  if (tid == 0) counters[rg] = 0;  // leave the ticket zeroed for the next call
 }
 
 // ---- host side ---------------------------------------------------------------
-
-static int draft_kpow2(int k) {
-  int K = 1;
-  while (K < k) K <<= 1;
-  return K;
-}
 
 int draft_splits(int B, int R, int V, int vec, int num_sms) {
   const int64_t rows = static_cast<int64_t>(B) * R;
@@ -359,35 +367,21 @@ int draft_splits(int B, int R, int V, int vec, int num_sms) {
 size_t draft_workspace_bytes(int B, int D, int k, int V, int vec, int num_sms) {
   const int R = 1 + (D - 1) * k;
   const int S = draft_splits(B, R, V, vec, num_sms);
-  const int K = draft_kpow2(k);
-  const size_t rec = 16 + 8 * static_cast<size_t>(K);
-  return draft_counter_bytes(B, R) + (S > 1 ? static_cast<size_t>(B) * R * S * rec : 0);
-}
-
-template <typename T, int K>
-static cudaError_t launch_tk(const DraftArgs &a, cudaStream_t st) {
-  static bool configured = false;  // the attribute is per function, set once
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(draft_topk_kernel<T, K>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kDraftSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  draft_topk_kernel<T, K><<<dim3(a.S, a.B * a.R), kDraftThreads, kDraftSmem, st>>>(a);
-  return cudaGetLastError();
+  if (S == 1) return draft_counter_bytes(B, R);
+  return draft_counter_bytes(B, R) + draft_ms_bytes(B, R, S) + static_cast<size_t>(B) * R * S * k * sizeof(uint64_t);
 }
 
 template <typename T>
 static cudaError_t launch_t(const DraftArgs &a, cudaStream_t st) {
-  switch (draft_kpow2(a.k)) {
-    case 1: return launch_tk<T, 1>(a, st);
-    case 2: return launch_tk<T, 2>(a, st);
-    case 4: return launch_tk<T, 4>(a, st);
-    case 8: return launch_tk<T, 8>(a, st);
-    case 16: return launch_tk<T, 16>(a, st);
-    case 32: return launch_tk<T, 32>(a, st);
-    default: return cudaErrorInvalidValue;
+  static bool configured = false;  // the attribute is per function, set once
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(draft_topk_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kDraftSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
   }
+  draft_topk_kernel<T><<<dim3(a.S, a.B * a.R), kDraftThreads, kDraftSmem, st>>>(a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_draft_topk(const void *logits, int dtype, int B, int D, int k, int V,

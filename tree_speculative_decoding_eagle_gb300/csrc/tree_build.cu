@@ -17,7 +17,7 @@
 
 namespace eagle {
 
-constexpr int kTreeThreads = 256;
+constexpr int kTreeThreads = 512;
 constexpr int kMaxGid = 4095;
 
 __device__ __forceinline__ uint64_t tree_key(float v, int pgid, int tok) {
@@ -41,22 +41,21 @@ struct TreeArgs {
 };
 
 // Count, for each of n_items items, how many keys of `set` exceed the item's
-// key; 8 lanes per item.  Must be called by the whole block.
+// key; 4 lanes per item.  Must be called by the whole block.
 __device__ __forceinline__ void count_greater(const uint64_t *item_keys, int n_items,
                                               const uint64_t *set, int n_set, int *out) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nwarps = blockDim.x >> 5;
-  for (int base = warp * 4; base < n_items; base += nwarps * 4) {
-    const int it = base + (lane >> 3);
-    const int sub = lane & 7;
+  for (int base = warp * 8; base < n_items; base += nwarps * 8) {
+    const int it = base + (lane >> 2);
+    const int sub = lane & 3;
     int cnt = 0;
     if (it < n_items) {
       const uint64_t me = item_keys[it];
-      for (int q = sub; q < n_set; q += 8) cnt += set[q] > me;
+      for (int q = sub; q < n_set; q += 4) cnt += set[q] > me;
     }
     cnt += __shfl_xor_sync(0xffffffffu, cnt, 1);
     cnt += __shfl_xor_sync(0xffffffffu, cnt, 2);
-    cnt += __shfl_xor_sync(0xffffffffu, cnt, 4);
     if (it < n_items && sub == 0) out[it] = cnt;
   }
 }
@@ -99,6 +98,8 @@ __global__ void __launch_bounds__(kTreeThreads) tree_build_kernel(TreeArgs a) {
   int *s_out = s_row + (NC + 1);                                 // [NC+1] gid -> node
   int *s_par = s_out + (NC + 1);                                 // [n]
   int *s_E = s_par + n;                                          // [k]
+  int *s_tok = s_E + k;                                          // [R*k] used rows
+  float *s_conf = reinterpret_cast<float *>(s_tok + (1 + (D - 1) * k) * k);
   __shared__ int s_bad;
 
   const int32_t *tok = a.tok + static_cast<int64_t>(b) * D * kk;
@@ -109,6 +110,20 @@ __global__ void __launch_bounds__(kTreeThreads) tree_build_kernel(TreeArgs a) {
     s_row[g] = -1;
     s_out[g] = -1;
   }
+  // used draft rows (slot 0 = row [0,0], slot 1+(d-1)k+j = row [d,j]) in one
+  // coalesced pass; tokens and confidences outside the domain are flagged and
+  // tokens clamped so the key fields stay in range
+  const int R = 1 + (D - 1) * k;
+  for (int idx = tid; idx < R * k; idx += blockDim.x) {
+    const int slot = idx / k, rr = idx % k;
+    const int gi = slot == 0 ? rr : ((1 + (slot - 1) / k) * k + (slot - 1) % k) * k + rr;
+    int t = tok[gi];
+    const float c = conf[gi];
+    if (!(c >= 0.f && c <= 1.f) || t < 0 || t > 0xFFFFF) s_bad = 1;
+    if (t < 0 || t > 0xFFFFF) t = 0;
+    s_tok[idx] = t;
+    s_conf[idx] = c;
+  }
   __syncthreads();
   if (tid == 0) {
     s_row[0] = 0;
@@ -117,12 +132,8 @@ __global__ void __launch_bounds__(kTreeThreads) tree_build_kernel(TreeArgs a) {
 
   // depth-1 layer: the root row's tokens
   for (int r = tid; r < k; r += blockDim.x) {
-    int t = tok[r];
-    float c = conf[r];
-    if (!(c >= 0.f && c <= 1.f) || t < 0 || t > 0xFFFFF) s_bad = 1;
-    if (t < 0 || t > 0xFFFFF) t = 0;  // keep the key's fields in range
-    c = __fadd_rn(__fmul_rn(1.0f, c), 0.0f);
-    s_key[1 + r] = tree_key(c, 0, t);
+    const float c = __fadd_rn(__fmul_rn(1.0f, s_conf[r]), 0.0f);
+    s_key[1 + r] = tree_key(c, 0, s_tok[r]);
   }
   int nL = 0, cur = 0;
   for (int d = 1; d <= D; ++d) {
@@ -167,12 +178,9 @@ __global__ void __launch_bounds__(kTreeThreads) tree_build_kernel(TreeArgs a) {
     for (int q = tid; q < kk; q += blockDim.x) {
       const int j = q / k, r = q % k;
       const int p = s_E[j];
-      int t = tok[(d * k + j) * k + r];
-      const float c = conf[(d * k + j) * k + r];
-      if (!(c >= 0.f && c <= 1.f) || t < 0 || t > 0xFFFFF) s_bad = 1;
-      if (t < 0 || t > 0xFFFFF) t = 0;
-      const float v = __fadd_rn(__fmul_rn(tkey_score(s_key[p]), c), 0.0f);
-      s_key[nbase + q] = tree_key(v, p, t);
+      const int slot = (1 + (d - 1) * k + j) * k + r;
+      const float v = __fadd_rn(__fmul_rn(tkey_score(s_key[p]), s_conf[slot]), 0.0f);
+      s_key[nbase + q] = tree_key(v, p, s_tok[slot]);
     }
   }
   __syncthreads();
@@ -242,7 +250,8 @@ size_t tree_smem_bytes(int D, int k, int m) {
                + sizeof(int) * 2 * m                  // s_Lg
                + sizeof(int) * (2 * kk + m)           // s_cnt
                + sizeof(int) * 2 * (NC + 1)           // s_row, s_out
-               + sizeof(int) * n + sizeof(int) * k;   // s_par, s_E
+               + sizeof(int) * n + sizeof(int) * k    // s_par, s_E
+               + 8 * static_cast<size_t>(1 + (D - 1) * k) * k;  // s_tok, s_conf
   return (bytes + 15) / 16 * 16;
 }
 
