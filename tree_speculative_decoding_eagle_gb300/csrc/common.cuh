@@ -70,6 +70,65 @@ template <> struct VecTraits<__nv_bfloat16> {
   }
 };
 
+// ---- packed fp32 pairs (sm_100 family: one instruction for two lanes) ------
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float &a, float &b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// Largest of the eight (bf16) or four (fp32) values of a 16-byte vector.
+template <typename T> __device__ __forceinline__ float vec_max(const uint4 &v);
+template <> __device__ __forceinline__ float vec_max<float>(const uint4 &v) {
+  return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
+               fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
+}
+template <> __device__ __forceinline__ float vec_max<__nv_bfloat16>(const uint4 &v) {
+  const __nv_bfloat162 a = __hmax2(*reinterpret_cast<const __nv_bfloat162 *>(&v.x),
+                                   *reinterpret_cast<const __nv_bfloat162 *>(&v.y));
+  const __nv_bfloat162 b = __hmax2(*reinterpret_cast<const __nv_bfloat162 *>(&v.z),
+                                   *reinterpret_cast<const __nv_bfloat162 *>(&v.w));
+  const __nv_bfloat162 c = __hmax2(a, b);
+  const uint32_t w = *reinterpret_cast<const uint32_t *>(&c);
+  return fmaxf(bf16_lo(w), bf16_hi(w));
+}
+
+// Sum over a 16-byte vector of 2^(x*log2e - mL), as a packed pair of partial
+// sums accumulated into acc.
+template <typename T> __device__ __forceinline__ uint64_t vec_exp_sum(const uint4 &v, uint64_t L2, uint64_t nmL2, uint64_t acc);
+template <> __device__ __forceinline__ uint64_t vec_exp_sum<__nv_bfloat16>(const uint4 &v, uint64_t L2, uint64_t nmL2,
+                                                                           uint64_t acc) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    float t0, t1;
+    f2_unpack(f2_fma(f2_pack(bf16_lo(w[q]), bf16_hi(w[q])), L2, nmL2), t0, t1);
+    acc = f2_add(acc, f2_pack(ex2_approx(t0), ex2_approx(t1)));
+  }
+  return acc;
+}
+template <> __device__ __forceinline__ uint64_t vec_exp_sum<float>(const uint4 &v, uint64_t L2, uint64_t nmL2,
+                                                                   uint64_t acc) {
+  float t0, t1;
+  f2_unpack(f2_fma(f2_pack(__uint_as_float(v.x), __uint_as_float(v.y)), L2, nmL2), t0, t1);
+  acc = f2_add(acc, f2_pack(ex2_approx(t0), ex2_approx(t1)));
+  f2_unpack(f2_fma(f2_pack(__uint_as_float(v.z), __uint_as_float(v.w)), L2, nmL2), t0, t1);
+  return f2_add(acc, f2_pack(ex2_approx(t0), ex2_approx(t1)));
+}
+
 // Streaming 16-byte load that does not allocate in L1.
 __device__ __forceinline__ uint4 ld_stream16(const void *p) {
   uint4 v;

@@ -5,10 +5,10 @@
 // used row: M = max, Z = sum exp(x - M), the k largest logits (ties -> lower
 // token id) and c = exp(x - M) / Z.
 //
-// One pass over HBM.  A row may be split across S CTAs (to fill the GPU when
-// there are few rows); each CTA streams its slice through a ring of shared-
-// memory stages filled by bulk copies and keeps an online (max, sum-exp) pair
-// per thread.  Top-k selection works on unique 64-bit keys (logit order, then
+// One pass over HBM.  A row is split into parts of 8 warps x 2048 tokens
+// (bf16; 1024 for fp32), one CTA per part.  Each warp holds its segment in
+// registers (all 16-byte loads in flight at once) and takes two passes over
+// them: lane maxima, then the sum of exp(x - lane max).  Top-k selection works on unique 64-bit keys (logit order, then
 // lower token id).  Every lane tracks its running maximum; the k-th largest
 // lane maximum of a warp (a 32-lane bitonic sort per chunk) bounds the top k
 // from below, and the block keeps the largest such bound.  Values at or
@@ -20,7 +20,6 @@
 // to finish (atomic ticket in the workspace) merges the S partial results;
 // no CTA ever waits for another.
 #include "common.cuh"
-#include "sm100.cuh"
 
 namespace eagle {
 
@@ -36,10 +35,7 @@ struct DraftArgs {
 };
 
 constexpr int kDraftThreads = 256;
-constexpr int kDraftUnroll = 4;                                // vectors per thread per chunk
-constexpr int kDraftChunkVec = kDraftThreads * kDraftUnroll;   // 16-byte vectors per chunk
-constexpr int kDraftStages = 4;                                // chunks in flight per CTA
-constexpr int kDraftSmem = kDraftStages * kDraftChunkVec * 16 + 128;
+constexpr int kDraftVecPerLane = 8;  // 16-byte vectors each lane holds in registers
 
 // Workspace: [tickets: u32 per row][(max, sum) per row and split][k keys per
 // row and split], each part 256-byte aligned.
@@ -92,10 +88,12 @@ __device__ __forceinline__ void warp_compact(uint64_t *wl, int *wn, uint64_t *bu
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kDraftThreads) draft_topk_kernel(DraftArgs a) {
+__global__ void __launch_bounds__(kDraftThreads, 3) draft_topk_kernel(DraftArgs a) {
   using VT = VecTraits<T>;
   constexpr int VEC = VT::kElems;
-  constexpr int CAP = 64 * VEC;  // candidate buffer per warp (two full vector steps)
+  constexpr int NVL = kDraftVecPerLane;
+  constexpr int SEG = 32 * NVL * VEC;  // tokens per warp
+  constexpr int CAP = 32 * VEC;        // candidate buffer per warp (one full vector step)
   constexpr int NW = kDraftThreads / 32;
   __shared__ uint64_t s_buf[NW][CAP];
   __shared__ uint64_t s_wl[NW][32], s_tmp[NW][32];
@@ -103,7 +101,6 @@ __global__ void __launch_bounds__(kDraftThreads) draft_topk_kernel(DraftArgs a) 
   __shared__ uint64_t s_top[32];
   __shared__ float s_m[NW], s_s[NW];
   __shared__ int s_last;
-  __shared__ volatile int s_abort;
   __shared__ unsigned s_thr;  // block prune bound (order-preserving bits)
 
   const int s = blockIdx.x;
@@ -118,96 +115,65 @@ __global__ void __launch_bounds__(kDraftThreads) draft_topk_kernel(DraftArgs a) 
 
   const T *row = reinterpret_cast<const T *>(a.logits) +
                  ((static_cast<int64_t>(b) * a.D + d) * a.k + j) * a.ld;
-  const int64_t NV = a.V / VEC;
-  const int64_t v0 = NV * s / a.S, v1 = NV * (s + 1) / a.S;
-  const int n_chunks = static_cast<int>((v1 - v0 + kDraftChunkVec - 1) / kDraftChunkVec);
-
-  // the slice streams through a ring of shared-memory stages filled by bulk
-  // copies (one elected thread), so many bytes are in flight per SM
-  extern __shared__ __align__(128) unsigned char dsm[];
-  uint4 *stage_buf = reinterpret_cast<uint4 *>(dsm);
-  uint64_t *full = reinterpret_cast<uint64_t *>(dsm + kDraftStages * kDraftChunkVec * 16);
-  if (tid == 0) {
-    s_abort = 0;
-    s_thr = ordered_u32(-INFINITY);
-    for (int q = 0; q < kDraftStages; ++q) sm100::mbar_init(&full[q], 1);
-    sm100::mbar_init_fence();
-  }
+  if (tid == 0) s_thr = ordered_u32(-INFINITY);
   if (lane == 0) s_wn[warp] = 0;
-  __syncthreads();
-  auto issue = [&](int c) {
-    const int64_t first = v0 + static_cast<int64_t>(c) * kDraftChunkVec;
-    const uint32_t nvec = static_cast<uint32_t>(min(static_cast<int64_t>(kDraftChunkVec), v1 - first));
-    uint64_t *bar = &full[c % kDraftStages];
-    sm100::mbar_arrive_expect_tx(bar, nvec * 16u);
-    sm100::bulk_load(stage_buf + (c % kDraftStages) * kDraftChunkVec, row + first * VEC, nvec * 16u, bar);
-  };
-  if (tid == 0)
-    for (int c = 0; c < min(kDraftStages, n_chunks); ++c) issue(c);
-
-  float m = -INFINITY, sum = 0.f;
-  float lmax = -INFINITY;  // this lane's largest value so far
-  float thr = -INFINITY;   // prune bound: at least k values of the slice are >= thr
-  int fill = 0;            // candidates waiting in the warp buffer
-  int consumed = 0;
-
-  for (int c = 0; c < n_chunks; ++c) {
-    const int st = c % kDraftStages;
-    if (!sm100::mbar_wait(&full[st], (c / kDraftStages) & 1, &s_abort)) report(a.status, EAGLE_ERR_TIMEOUT);
-    const int64_t first = v0 + static_cast<int64_t>(c) * kDraftChunkVec;
-    const int nvec = static_cast<int>(min(static_cast<int64_t>(kDraftChunkVec), v1 - first));
-    const uint4 *src = stage_buf + st * kDraftChunkVec;
-    uint4 vb[kDraftUnroll];
-    float vmx[kDraftUnroll];
+  __syncthreads();  // s_thr and list sizes initialised
+  // This CTA's part of the row is a range of 2048-token segments (1024 for
+  // fp32); warp w takes segments w, w+8, ...  A segment is held in
+  // registers (all 16-byte loads in flight together) and visited twice:
+  // lane maxima, then the sum of exp(x - segment lane max).
+  const int nseg = (a.V + SEG - 1) / SEG;
+  const int spp = (nseg + a.S - 1) / a.S;
+  const int g0 = s * spp, g1 = min(nseg, g0 + spp);
+  float m = -INFINITY, sum = 0.f;  // this lane's running max and sum of exp(x - m)
+  float lmax = -INFINITY;          // this lane's largest value so far
+  float thr = -INFINITY;           // prune bound: at least k values of the part are >= thr
+  int fill = 0;
+  for (int gseg = g0 + warp; gseg < g1; gseg += NW) {
+    const int seg0 = gseg * SEG;
+    const int nvec = min(SEG, a.V - seg0) / VEC;
+    uint4 vb[NVL];
 #pragma unroll
-    for (int u = 0; u < kDraftUnroll; ++u) {
-      const int iv = u * kDraftThreads + tid;
-      vmx[u] = -INFINITY;
-      if (iv < nvec && !s_abort) {
-        vb[u] = src[iv];
-        float x[VEC];
-        VT::unpack(vb[u], x);
-        float vmax = x[0];
-#pragma unroll
-        for (int e = 1; e < VEC; ++e) vmax = fmaxf(vmax, x[e]);
-        vmx[u] = vmax;
-        if (vmax > -INFINITY) {
-          if (vmax > m) {
-            sum *= ex2_approx((m - vmax) * kLog2e);
-            m = vmax;
-          }
-          const float mL = m * kLog2e;
-          float p[VEC];
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) p[e] = ex2_approx(fmaf(x[e], kLog2e, -mL));
-#pragma unroll
-          for (int w2 = VEC / 2; w2 > 0; w2 >>= 1)  // pairwise within the vector
-#pragma unroll
-            for (int e = 0; e < w2; ++e) p[e] += p[e + w2];
-          sum += p[0];
-        }
-        lmax = fmaxf(lmax, vmax);
-      }
+    for (int i = 0; i < NVL; ++i) {
+      const int v = lane + 32 * i;
+      if (v < nvec) vb[i] = ld_stream16(row + seg0 + v * VEC);
     }
-    // Lane maxima are distinct elements, so the k-th largest of the warp's
-    // lane maxima has at least k elements at or above it; so has any other
-    // warp's bound and the k-th key of a full warp list.  The block keeps the
-    // largest bound.
+    float smax = -INFINITY;
+    float vmx[NVL];
+#pragma unroll
+    for (int i = 0; i < NVL; ++i) {
+      vmx[i] = (lane + 32 * i < nvec) ? vec_max<T>(vb[i]) : -INFINITY;
+      smax = fmaxf(smax, vmx[i]);
+    }
+    if (smax > -INFINITY) {
+      const float mL = smax * kLog2e;
+      const uint64_t L2 = f2_pack(kLog2e, kLog2e), nmL2 = f2_pack(-mL, -mL);
+      uint64_t acc = f2_pack(0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < NVL; ++i)
+        if (lane + 32 * i < nvec) acc = vec_exp_sum<T>(vb[i], L2, nmL2, acc);
+      float a0, a1;
+      f2_unpack(acc, a0, a1);
+      lse_combine(m, sum, smax, a0 + a1);
+    }
+    lmax = fmaxf(lmax, smax);
+    // Lane maxima are distinct elements, so the k-th largest lane maximum of
+    // the warp has at least k elements at or above it; the k-th key of a full
+    // warp list too.  The block keeps the largest such bound.
     {
       const float y = warp_sort_desc(lmax, lane);
       float tw = __shfl_sync(0xffffffffu, y, k - 1);
       if (s_wn[warp] == k) tw = fmaxf(tw, key_value(wl[k - 1]));
-      if (tw > -INFINITY) atomicMax(&s_thr, ordered_u32(tw));
-      thr = fmaxf(thr, fmaxf(tw, from_ordered_u32(s_thr)));
+      if (lane == 0 && tw > -INFINITY) atomicMax(&s_thr, ordered_u32(tw));
+      thr = fmaxf(thr, fmaxf(tw, from_ordered_u32(*const_cast<volatile unsigned *>(&s_thr))));
     }
 #pragma unroll
-    for (int u = 0; u < kDraftUnroll; ++u) {
-      const int iv = u * kDraftThreads + tid;
-      const bool maybe = vmx[u] > -INFINITY && vmx[u] >= thr;
+    for (int i = 0; i < NVL; ++i) {
+      const bool maybe = vmx[i] > -INFINITY && vmx[i] >= thr;
       if (__any_sync(0xffffffffu, maybe)) {
         unsigned cm = 0;
         float x[VEC];
-        VT::unpack(vb[u], x);
+        VT::unpack(vb[i], x);
         if (maybe) {
 #pragma unroll
           for (int e = 0; e < VEC; ++e)
@@ -227,7 +193,7 @@ __global__ void __launch_bounds__(kDraftThreads) draft_topk_kernel(DraftArgs a) 
         }
         if (cm) {
           int pos = fill + incl - cnt;
-          const uint32_t t0 = static_cast<uint32_t>((first + iv) * VEC);
+          const uint32_t t0 = static_cast<uint32_t>(seg0 + (lane + 32 * i) * VEC);
 #pragma unroll
           for (int e = 0; e < VEC; ++e)
             if ((cm >> e) & 1u) buf[pos++] = topk_key(x[e], t0 + e);
@@ -235,19 +201,6 @@ __global__ void __launch_bounds__(kDraftThreads) draft_topk_kernel(DraftArgs a) 
         fill += total;
       }
     }
-    consumed = c + 1;
-    __syncthreads();  // every thread is done with this stage
-    if (s_abort) break;
-    if (tid == 0 && c + kDraftStages < n_chunks) issue(c + kDraftStages);
-  }
-  if (s_abort) {
-    // drain the copies still in flight before the CTA's shared memory goes away
-    if (tid == 0) {
-      volatile int never = 0;
-      for (int c = max(0, consumed - 1); c < min(n_chunks, consumed - 1 + kDraftStages); ++c)
-        sm100::mbar_wait(&full[c % kDraftStages], (c / kDraftStages) & 1, &never, 100000000ull);
-    }
-    return;
   }
   if (fill > 0) warp_compact(wl, &s_wn[warp], buf, fill, s_tmp[warp], k, lane);
 
@@ -350,15 +303,15 @@ __global__ void __launch_bounds__(kDraftThreads) draft_topk_kernel(DraftArgs a) 
 
 // ---- host side ---------------------------------------------------------------
 
+// Parts (CTAs) per row: enough CTAs for about three per SM, but no part
+// smaller than one 2048-token segment per warp.
 int draft_splits(int B, int R, int V, int vec, int num_sms) {
   const int64_t rows = static_cast<int64_t>(B) * R;
-  const int64_t NV = V / vec;
-  const int64_t target = static_cast<int64_t>(num_sms) * 2;  // two CTAs fit per SM
-  int64_t S = (target + rows - 1) / rows;
-  // keep at least two full vector sweeps of the block per split
-  int64_t max_by_len = NV / (2 * kDraftThreads);
-  if (max_by_len < 1) max_by_len = 1;
-  if (S > max_by_len) S = max_by_len;
+  const int seg = kDraftVecPerLane * 32 * vec;
+  const int64_t nseg = (V + seg - 1) / seg;
+  const int64_t max_parts = (nseg + (kDraftThreads / 32) - 1) / (kDraftThreads / 32);
+  int64_t S = (static_cast<int64_t>(num_sms) * 3 + rows - 1) / rows;
+  if (S > max_parts) S = max_parts;
   if (S > 32) S = 32;
   if (S < 1) S = 1;
   return static_cast<int>(S);
@@ -373,14 +326,7 @@ size_t draft_workspace_bytes(int B, int D, int k, int V, int vec, int num_sms) {
 
 template <typename T>
 static cudaError_t launch_t(const DraftArgs &a, cudaStream_t st) {
-  static bool configured = false;  // the attribute is per function, set once
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(draft_topk_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kDraftSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  draft_topk_kernel<T><<<dim3(a.S, a.B * a.R), kDraftThreads, kDraftSmem, st>>>(a);
+  draft_topk_kernel<T><<<dim3(a.S, a.B * a.R), kDraftThreads, 0, st>>>(a);
   return cudaGetLastError();
 }
 
