@@ -6,20 +6,23 @@
 // the [EAGLE-2] mask (section "注意マスクの調整") node i attends to the
 // prefix and to its own ancestors only.
 //
-// One CTA per (sequence b, KV head g, group of MT M-tiles, KV split).  Query
-// rows are (node, head-in-group) pairs, so the m+1 nodes x G grouped heads of
-// a KV head share every K/V tile.  Key tiles are 64 keys: first the prefix
-// (positions 0..kv_len-1), then the tree nodes, whose tile is masked with the
+// One CTA per (sequence b, KV head g, group of MT 128-row M-tiles, KV split).
+// Query rows are (node, head-in-group) pairs, so the m+1 nodes x G grouped
+// heads of a KV head share every K/V tile.  Key tiles hold NK keys: first the
+// prefix (positions 0..kv_len-1), then the tree nodes, masked with the
 // ancestor bits.  Roles:
 //   * producer warp: K/V tiles into a ring of shared-memory stages, by TMA
 //     (128-byte swizzle) for full tiles, by plain loads with zero fill for
 //     the ragged last prefix tile;
-//   * MMA warp (one elected thread): S_t = Q_t K^T and O_t += P_t V with
-//     tcgen05.mma, accumulators in tensor memory, completion via
-//     tcgen05.commit on mbarriers;
-//   * one softmax warpgroup per M-tile: reads its S rows from tensor memory,
-//     online softmax in fp32 (base-2), writes P (bf16) to swizzled shared
-//     memory, rescales its O rows in tensor memory when the row max grows.
+//   * MMA warp (one elected thread): S_t = Q_t K^T (A = Q from shared
+//     memory) and O_t += P_t V (A = P from tensor memory), accumulators in
+//     tensor memory, completion via tcgen05.commit on mbarriers; S of the
+//     next tile is issued before P.V of the current one;
+//   * one softmax warpgroup per M-tile: reads its S rows from tensor memory
+//     (a max pass, then an exponent pass), writes P as packed bf16 pairs into
+//     tensor memory, keeps the row sum, and rescales its O rows in tensor
+//     memory only when the running maximum grows by more than 2^8.
+// Tensor memory per M-tile: S (NK columns), P (NK/2), O (dh).
 // Every wait is bounded; a timeout raises EAGLE_ERR_TIMEOUT in the status
 // word and the CTA drains its copies and MMAs, frees tensor memory and exits.
 #include <mutex>
@@ -30,8 +33,6 @@
 namespace eagle {
 
 using namespace sm100;
-
-constexpr int kNK = 64;  // keys per tile
 
 struct TcArgs {
   const __nv_bfloat16 *q, *k_cache, *v_cache;
@@ -45,32 +46,36 @@ struct TcArgs {
   int32_t *status;
 };
 
-template <int DH, int MT, int STAGES>
+template <int DH, int MT, int NK, int STAGES>
 struct TcShape {
-  static constexpr int kRegions = DH / 64;
-  static constexpr int kQBytes = MT * kRegions * 16384;
-  static constexpr int kPBytes = MT * 16384;
-  static constexpr int kTileBytes = kRegions * 8192;        // one K (or V) tile
+  static constexpr int kRegions = DH / 64;                   // 128-byte swizzle atoms per row
+  static constexpr int kQBytes = MT * kRegions * 16384;      // 128 rows x dh per M-tile
+  static constexpr int kTileBytes = kRegions * NK * 128;     // one K (or V) tile
   static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kBarOff = kQBytes + kPBytes + STAGES * kStageBytes;
+  static constexpr int kBarOff = kQBytes + STAGES * kStageBytes;
   static constexpr int kNumBars = 2 * STAGES + 4 * MT + 1;
   static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;  // + alignment slack
   static constexpr int kThreads = MT * 128 + 64;
-  static constexpr int kTmemCols = MT * (kNK + DH) <= 128 ? 128 : (MT * (kNK + DH) <= 256 ? 256 : 512);
+  static constexpr int kColS = 0;                            // S_t at t*NK
+  static constexpr int kColP = MT * NK;                      // P_t at kColP + t*NK/2
+  static constexpr int kColO = MT * NK + MT * NK / 2;        // O_t at kColO + t*DH
+  static constexpr int kCols = kColO + MT * DH;
+  static constexpr int kTmemCols = kCols <= 128 ? 128 : (kCols <= 256 ? 256 : 512);
+  static_assert(kCols <= 512, "tensor memory budget");
 };
 
-template <int DH, int MT, int STAGES>
+template <int DH, int MT, int NK, int STAGES>
 __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
     tree_attn_tc_kernel(const __grid_constant__ CUtensorMap kc_map, const __grid_constant__ CUtensorMap vc_map,
                         const __grid_constant__ CUtensorMap kt_map, const __grid_constant__ CUtensorMap vt_map,
                         TcArgs a) {
-  using Sh = TcShape<DH, MT, STAGES>;
+  using Sh = TcShape<DH, MT, NK, STAGES>;
+  constexpr int NH = NK / 64;  // 64-key halves of a tile
   extern __shared__ unsigned char raw_smem[];
   unsigned char *sm = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(raw_smem) + 1023) & ~static_cast<uintptr_t>(1023));
   unsigned char *sQ = sm;
-  unsigned char *sP = sm + Sh::kQBytes;
-  unsigned char *sKV = sP + Sh::kPBytes;
+  unsigned char *sKV = sm + Sh::kQBytes;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + Sh::kBarOff);
   uint64_t *kv_full = bars;
   uint64_t *kv_empty = bars + STAGES;
@@ -87,11 +92,11 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
   const int bg = blockIdx.z, b = bg / a.Hkv, g = bg % a.Hkv;
   const int n = a.n;
   const int L = min(max(a.kv_len[b], 0), a.Lmax);
-  const int n_ptiles = (L + kNK - 1) / kNK;
+  const int n_ptiles = (L + NK - 1) / NK;
   const int tps = (n_ptiles + a.S - 1) / a.S;
   const int p0 = min(n_ptiles, split * tps), p1 = min(n_ptiles, p0 + tps);
   const int np = p1 - p0;
-  const int ntt = (split == a.S - 1) ? (n + kNK - 1) / kNK : 0;
+  const int ntt = (split == a.S - 1) ? (n + NK - 1) / NK : 0;
   const int T = np + ntt;  // key tiles of this CTA
   const int producer_warp = MT * 4, mma_warp = MT * 4 + 1;
 
@@ -151,9 +156,9 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
       unsigned char *kst = sKV + st * Sh::kStageBytes;
       unsigned char *vst = kst + Sh::kTileBytes;
       const bool prefix = j < np;
-      const int key0 = prefix ? (p0 + j) * kNK : (j - np) * kNK;
-      const int valid = prefix ? min(kNK, L - key0) : kNK;
-      if (!prefix || valid == kNK) {
+      const int key0 = prefix ? (p0 + j) * NK : (j - np) * NK;
+      const int valid = prefix ? min(NK, L - key0) : NK;
+      if (!prefix || valid == NK) {
         if (lane == 0) {
           mbar_arrive_expect_tx(&kv_full[st], Sh::kStageBytes);
           const CUtensorMap *km = prefix ? &kc_map : &kt_map;
@@ -161,8 +166,8 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
           const int row0 = prefix ? bg * a.Lmax + key0 : bg * n + key0;
 #pragma unroll
           for (int r = 0; r < Sh::kRegions; ++r) {
-            tma_load_2d(kst + r * 8192, km, r * 64, row0, &kv_full[st]);
-            tma_load_2d(vst + r * 8192, vm, r * 64, row0, &kv_full[st]);
+            tma_load_2d(kst + r * NK * 128, km, r * 64, row0, &kv_full[st]);
+            tma_load_2d(vst + r * NK * 128, vm, r * 64, row0, &kv_full[st]);
           }
         }
       } else {
@@ -170,14 +175,14 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
         // kv_len is never read)
         const __nv_bfloat16 *kg = a.k_cache + (static_cast<int64_t>(bg) * a.Lmax + key0) * DH;
         const __nv_bfloat16 *vg = a.v_cache + (static_cast<int64_t>(bg) * a.Lmax + key0) * DH;
-        for (int idx = lane; idx < kNK * (DH / 8); idx += 32) {
+        for (int idx = lane; idx < NK * (DH / 8); idx += 32) {
           const int r = idx / (DH / 8), c = idx % (DH / 8);
           uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
           if (r < valid) {
             kv = *reinterpret_cast<const uint4 *>(kg + r * DH + c * 8);
             vv = *reinterpret_cast<const uint4 *>(vg + r * DH + c * 8);
           }
-          const uint32_t off = (c / 8) * 8192 + sw128_offset(r, c % 8);
+          const uint32_t off = (c / 8) * (NK * 128) + sw128_offset(r, c % 8);
           *reinterpret_cast<uint4 *>(kst + off) = kv;
           *reinterpret_cast<uint4 *>(vst + off) = vv;
         }
@@ -190,10 +195,10 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
   } else if (warp == mma_warp) {
     // --------------------------------------------------------------------- MMA
     if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16(128, kNK, false);
+      constexpr uint32_t id_s = idesc_bf16(128, NK, false);
       constexpr uint32_t id_o = idesc_bf16(128, DH, true);
-      // S for tile j+1 is issued as soon as the softmax has read tile j's S,
-      // so it overlaps that softmax; P.V for tile j follows its P.
+      // S for tile j+1 is issued as soon as the softmax is done with tile j's
+      // S, so it overlaps that softmax's tail; P.V for tile j follows its P.
       auto issue_s = [&](int j) -> bool {
         const int st = j % STAGES;
         if (!mbar_wait(&kv_full[st], (j / STAGES) & 1, abort_flag)) return false;
@@ -206,8 +211,8 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
 #pragma unroll
           for (int s = 0; s < DH / 16; ++s) {
             const uint64_t ad = sdesc_sw128(qaddr + (s / 4) * 16384 + (s % 4) * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(kaddr + (s / 4) * 8192 + (s % 4) * 32, 16, 1024);
-            mma_bf16_ss(tmem + t * kNK, ad, bd, id_s, s > 0);
+            const uint64_t bd = sdesc_sw128(kaddr + (s / 4) * (NK * 128) + (s % 4) * 32, 16, 1024);
+            mma_bf16_ss(tmem + Sh::kColS + t * NK, ad, bd, id_s, s > 0);
           }
           mma_commit(&s_full[t]);
         }
@@ -221,12 +226,11 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
         for (int t = 0; t < MT && ok; ++t) {
           if (!mbar_wait(&p_full[t], j & 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t paddr = smem_u32(sP + t * 16384);
+          const uint32_t pcol = tmem + Sh::kColP + t * (NK / 2);
 #pragma unroll
-          for (int s = 0; s < kNK / 16; ++s) {
-            const uint64_t ad = sdesc_sw128(paddr + s * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(vaddr + s * 2048, 8192, 1024);
-            mma_bf16_ss(tmem + MT * kNK + t * DH, ad, bd, id_o, (j > 0 || s > 0));
+          for (int s = 0; s < NK / 16; ++s) {
+            const uint64_t bd = sdesc_sw128(vaddr + s * 2048, NK * 128, 1024);
+            mma_bf16_ts(tmem + Sh::kColO + t * DH, pcol + s * 8, bd, id_o, (j > 0 || s > 0));
           }
           mma_commit(&o_done[t]);
         }
@@ -242,9 +246,9 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
     const int i = row_ok ? rho / a.G : 0;
     const int hh = row_ok ? rho % a.G : 0;
     const uint32_t lane_base = static_cast<uint32_t>(qtr * 32) << 16;
-    const uint32_t tS = tmem + lane_base + t * kNK;
-    const uint32_t tO = tmem + lane_base + MT * kNK + t * DH;
-    unsigned char *prow = sP + t * 16384;
+    const uint32_t tS = tmem + lane_base + Sh::kColS + t * NK;
+    const uint32_t tP = tmem + lane_base + Sh::kColP + t * (NK / 2);
+    const uint32_t tO = tmem + lane_base + Sh::kColO + t * DH;
     const uint64_t *mrow = a.mask + (static_cast<int64_t>(b) * n + i) * a.W;
     // m is the exponent base of this row's P and O (scaled, base-2 units).  It
     // is raised only when the row maximum exceeds it by more than 8, so P
@@ -254,61 +258,80 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
     for (int j = 0; j < T; ++j) {
       if (!warp_wait(&s_full[t], j & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
-      float sv[kNK];
-      tmem_ld64(tS, sv);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[t]);  // S stays in registers
-      // key validity: prefix positions below kv_len; tree nodes that are
-      // ancestors-or-self of this row's node
+      // key validity per 64-key half: prefix positions below kv_len; tree
+      // nodes that are ancestors-or-self of this row's node
       const bool prefix = j < np;
-      uint64_t keep;
-      if (prefix) {
-        const int valid = min(kNK, L - (p0 + j) * kNK);
-        keep = valid >= 64 ? ~0ull : ((1ull << valid) - 1ull);
-      } else {
-        keep = row_ok ? mrow[j - np] : 0ull;
-      }
-      const bool dense = __all_sync(0xffffffffu, keep == ~0ull);
-      if (!dense) {
+      uint64_t keep[NH];
 #pragma unroll
-        for (int c = 0; c < kNK; ++c) sv[c] = ((keep >> c) & 1ull) ? sv[c] : -INFINITY;
+      for (int h = 0; h < NH; ++h) {
+        if (prefix) {
+          const int valid = min(NK, L - (p0 + j) * NK) - 64 * h;
+          keep[h] = valid >= 64 ? ~0ull : (valid <= 0 ? 0ull : ((1ull << valid) - 1ull));
+        } else {
+          const int w = (j - np) * NH + h;
+          keep[h] = (row_ok && w < a.W) ? mrow[w] : 0ull;
+        }
       }
-      float mx[4] = {sv[0], sv[1], sv[2], sv[3]};
+      bool dense = true;
 #pragma unroll
-      for (int c = 4; c < kNK; c += 8) {
-        mx[0] = fmax3(mx[0], sv[c], sv[c + 4]);
-        mx[1] = fmax3(mx[1], sv[c + 1], sv[c + 5]);
-        mx[2] = fmax3(mx[2], sv[c + 2], sv[c + 6]);
-        mx[3] = fmax3(mx[3], sv[c + 3], sv[c + 7]);
+      for (int h = 0; h < NH; ++h) dense = dense && keep[h] == ~0ull;
+      dense = __all_sync(0xffffffffu, dense);
+      // pass 1: masked maximum of the row's scores
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        float sv[64];
+        tmem_ld64(tS + 64 * h, sv);
+        if (!dense) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) sv[c] = ((keep[h] >> c) & 1ull) ? sv[c] : -INFINITY;
+        }
+        float mx[4] = {sv[0], sv[1], sv[2], sv[3]};
+#pragma unroll
+        for (int c = 4; c < 64; c += 8) {
+          mx[0] = fmax3(mx[0], sv[c], sv[c + 4]);
+          mx[1] = fmax3(mx[1], sv[c + 1], sv[c + 5]);
+          mx[2] = fmax3(mx[2], sv[c + 2], sv[c + 6]);
+          mx[3] = fmax3(mx[3], sv[c + 3], sv[c + 7]);
+        }
+        tmax = fmax3(tmax, fmax3(mx[0], mx[1], mx[2]), mx[3]);
       }
-      const float tmax = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]) * a.scale_log2;  // scale > 0
+      tmax *= a.scale_log2;  // scale > 0
       const bool raise = tmax > m + 8.f;
       const float base = raise ? tmax : m;
       const float alpha = raise ? ex2_approx(m - tmax) : 1.f;  // m = -inf gives 0
       m = base;
-      if (j > 0) {  // P of the previous tile has been consumed, O is final for it
+      if (j > 0) {  // P.V of the previous tile is done: P is free, O is final for it
         if (!warp_wait(&o_done[t], (j - 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
       }
-      // P = exp2(s*scale - base) as bf16 into the 128B-swizzled K-major tile
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
-      // a row with no valid key yet has base -inf and only -inf scores: any
-      // finite exponent base then gives 0
+      // pass 2: P = exp2(s*scale - base), packed bf16 pairs into tensor memory
+      // (a row with no valid key yet has base -inf and only -inf scores: any
+      // finite exponent base then gives 0)
       const float nb = base > -INFINITY ? -base : 0.f;
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c8 = 0; c8 < kNK / 8; ++c8) {
-        float pv[8];
+      for (int h = 0; h < NH; ++h) {
+        float sv[64];
+        tmem_ld64(tS + 64 * h, sv);
+        if (!dense) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          pv[e] = ex2_approx(fmaf(sv[c8 * 8 + e], a.scale_log2, nb));  // -inf gives 0
-          ps[e & 3] += pv[e];
+          for (int c = 0; c < 64; ++c) sv[c] = ((keep[h] >> c) & 1ull) ? sv[c] : -INFINITY;
         }
-        __nv_bfloat162 h2[4];
+        float pk[32];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) h2[e] = __floats2bfloat162_rn(pv[2 * e], pv[2 * e + 1]);
-        *reinterpret_cast<uint4 *>(prow + sw128_offset(r, c8)) = *reinterpret_cast<const uint4 *>(h2);
+        for (int c = 0; c < 32; ++c) {
+          const float p0v = ex2_approx(fmaf(sv[2 * c], a.scale_log2, nb));
+          const float p1v = ex2_approx(fmaf(sv[2 * c + 1], a.scale_log2, nb));
+          ps[c & 3] += p0v + p1v;
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(p0v, p1v);
+          pk[c] = *reinterpret_cast<const float *>(&h2);
+        }
+        tmem_st32(tP + 32 * h, pk);
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[t]);  // S has been read
       l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
       if (j > 0 && __any_sync(0xffffffffu, raise)) {
 #pragma unroll
@@ -320,7 +343,6 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
           tmem_st32(tO + c0, o);
         }
       }
-      fence_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[t]);
@@ -409,13 +431,14 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2D bf16 tensor [rows, dh] viewed in 64 x 64 boxes with 128-byte swizzle.
-static bool make_kv_map(CUtensorMap *map, const void *base, int64_t rows, int dh) {
+// 2D bf16 tensor [rows, dh] viewed in boxes of 64 columns x `box_rows` rows
+// with 128-byte swizzle.
+static bool make_kv_map(CUtensorMap *map, const void *base, int64_t rows, int dh, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(dh), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(dh) * 2};
-  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kNK)};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -423,24 +446,24 @@ static bool make_kv_map(CUtensorMap *map, const void *base, int64_t rows, int dh
 }
 
 struct TcPlan {
-  int MT, mgroups, S, stages;
+  int MT, NK, mgroups, S, ctas_per_sm;
 };
 
-// Launch plan: M-tiles per CTA, and the KV split S chosen to minimise
-// (waves of CTAs) x (key tiles per CTA + the extra traffic a split's partial
-// results cost, in key-tile units).
+// Launch plan: M-tiles per CTA, key-tile width, and the KV split S chosen to
+// minimise (waves of CTAs) x (key tiles per CTA + the extra traffic a split's
+// partial results cost, in key-tile units).
 static TcPlan tc_plan(int B, int n, int Hq, int Hkv, int dh, int Lmax, int num_sms) {
   TcPlan p;
   const int G = Hq / Hkv;
   const int tiles = (n * G + 127) / 128;
-  p.MT = tiles <= 1 ? 1 : (tiles <= 2 || dh == 128) ? 2 : 4;
+  p.MT = tiles <= 1 ? 1 : 2;
+  p.NK = dh == 64 ? 128 : 64;
   p.mgroups = (tiles + p.MT - 1) / p.MT;
-  p.stages = 4;
+  p.ctas_per_sm = p.MT == 1 ? 2 : 1;
   const int64_t base = static_cast<int64_t>(B) * Hkv * p.mgroups;
-  const int ctas_per_sm = p.MT == 1 ? 2 : 1;
-  const int64_t slots = static_cast<int64_t>(num_sms) * ctas_per_sm;
-  const int64_t ptiles = (Lmax + kNK - 1) / kNK;
-  const double split_cost = static_cast<double>(G) * n / 32.0 / p.mgroups;
+  const int64_t slots = static_cast<int64_t>(num_sms) * p.ctas_per_sm;
+  const int64_t ptiles = (Lmax + p.NK - 1) / p.NK;
+  const double split_cost = static_cast<double>(G) * n * 64.0 / p.NK / 32.0 / p.mgroups;
   int best = 1;
   double best_cost = 1e30;
   for (int S = 1; S <= 32 && S <= ptiles; ++S) {
@@ -465,27 +488,22 @@ size_t attn_tc_workspace_bytes(int B, int n, int Hq, int Hkv, int dh, int Lmax, 
 cudaError_t launch_attn_combine_bf16(const float *part_o, const float *part_ml, int B, int n, int Hq, int dh,
                                      int S, void *out, float *lse, cudaStream_t st);
 
-// Stages of the K/V ring: single-tile dh=128 CTAs keep two stages so that two
-// CTAs fit in one SM's shared memory.
-template <int DH, int MT>
-constexpr int tc_stages() { return (DH == 128 && MT == 1) ? 2 : 4; }
-template <int DH, int MT>
-constexpr int tc_ctas_per_sm() { return MT == 1 ? 2 : 1; }
-
-template <int DH, int MT>
+template <int DH, int MT, int NK, int STAGES>
 static cudaError_t launch_tc_t(const CUtensorMap *maps, const TcArgs &a, const TcPlan &p, cudaStream_t st) {
-  constexpr int STAGES = tc_stages<DH, MT>();
-  using Sh = TcShape<DH, MT, STAGES>;
+  using Sh = TcShape<DH, MT, NK, STAGES>;
   static_assert(Sh::kSmem <= 232448, "shared memory budget");
+  // MT = 1 variants run two CTAs per SM (228 KB per SM, 1 KB reserved per CTA)
+  static_assert(MT != 1 || 2 * (Sh::kSmem + 1024) <= 233472, "two CTAs per SM");
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(tree_attn_tc_kernel<DH, MT, STAGES>,
+    cudaError_t e = cudaFuncSetAttribute(tree_attn_tc_kernel<DH, MT, NK, STAGES>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   dim3 grid(p.S, p.mgroups, a.B * a.Hkv);
-  tree_attn_tc_kernel<DH, MT, STAGES><<<grid, Sh::kThreads, Sh::kSmem, st>>>(maps[0], maps[1], maps[2], maps[3], a);
+  tree_attn_tc_kernel<DH, MT, NK, STAGES><<<grid, Sh::kThreads, Sh::kSmem, st>>>(maps[0], maps[1], maps[2],
+                                                                                maps[3], a);
   return cudaGetLastError();
 }
 
@@ -497,9 +515,9 @@ cudaError_t launch_tree_attn_tc(const void *q, const void *k_cache, const void *
   CUtensorMap maps[4];
   const int64_t cache_rows = static_cast<int64_t>(B) * Hkv * Lmax;
   const int64_t tree_rows = static_cast<int64_t>(B) * Hkv * n;
-  if (!make_kv_map(&maps[0], k_cache, cache_rows > 0 ? cache_rows : 1, dh) ||
-      !make_kv_map(&maps[1], v_cache, cache_rows > 0 ? cache_rows : 1, dh) ||
-      !make_kv_map(&maps[2], k_tree, tree_rows, dh) || !make_kv_map(&maps[3], v_tree, tree_rows, dh))
+  if (!make_kv_map(&maps[0], k_cache, cache_rows > 0 ? cache_rows : 1, dh, p.NK) ||
+      !make_kv_map(&maps[1], v_cache, cache_rows > 0 ? cache_rows : 1, dh, p.NK) ||
+      !make_kv_map(&maps[2], k_tree, tree_rows, dh, p.NK) || !make_kv_map(&maps[3], v_tree, tree_rows, dh, p.NK))
     return cudaErrorInvalidValue;
   TcArgs a;
   a.q = reinterpret_cast<const __nv_bfloat16 *>(q);
@@ -516,11 +534,11 @@ cudaError_t launch_tree_attn_tc(const void *q, const void *k_cache, const void *
   a.part_ml = a.part_o + static_cast<size_t>(B) * Hq * p.S * n * dh;
   a.status = status;
   cudaError_t e;
+  // stages: as many as shared memory allows at the variant's CTAs per SM
   if (dh == 64) {
-    e = p.MT == 1 ? launch_tc_t<64, 1>(maps, a, p, st)
-                  : p.MT == 2 ? launch_tc_t<64, 2>(maps, a, p, st) : launch_tc_t<64, 4>(maps, a, p, st);
+    e = p.MT == 1 ? launch_tc_t<64, 1, 128, 2>(maps, a, p, st) : launch_tc_t<64, 2, 128, 4>(maps, a, p, st);
   } else {
-    e = p.MT == 1 ? launch_tc_t<128, 1>(maps, a, p, st) : launch_tc_t<128, 2>(maps, a, p, st);
+    e = p.MT == 1 ? launch_tc_t<128, 1, 64, 2>(maps, a, p, st) : launch_tc_t<128, 2, 64, 4>(maps, a, p, st);
   }
   if (e != cudaSuccess || p.S == 1) return e;
   return launch_attn_combine_bf16(a.part_o, a.part_ml, B, n, Hq, dh, p.S, out, lse, st);
