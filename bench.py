@@ -43,6 +43,8 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--workload", default=MAIN_WORKLOAD)
+    p.add_argument("--batch", type=int, default=None,
+                   help="run the workload at this batch size instead of its own (small ncu captures)")
     p.add_argument("--also", default=ALSO_WORKLOAD, help="second workload reported in the line ('none' to skip)")
     p.add_argument("--impl", default="ours", choices=("ours", "reference"))
     p.add_argument("--no-e2e", action="store_true")
@@ -71,6 +73,16 @@ def algorithmic(w, kv_len, depth_sum):
     flops = 4 * w.dh * w.Hq // w.Hkv * w.Hkv * keys       # QK^T and PV, 2 flops per MAC
     return {"draft_topk": draft, "tree_build": 0, "tree_attn": attn, "verify": target,
             "attn_flops": flops, "total": draft + target + attn}
+
+
+def launches_per_step(w):
+    """Kernels one step launches: draft top-k 1, tree build (mask fused) 1,
+    tree attention 1 (+1 combine when the KV prefix is split, i.e. when it
+    asks for a workspace), verification 2 (chunk statistics, walk)."""
+    import tree_speculative_decoding_eagle_gb300 as eg
+    dt = eg.BF16 if w.dtype == "bf16" else eg.F32
+    split = eg.load_library().eagle_tree_attn_workspace_size(dt, w.B, w.n_nodes, w.Hq, w.Hkv, w.dh, w.L) > 0
+    return {"draft_topk": 1, "tree_build": 1, "tree_attn": 2 if split else 1, "verify": 2}
 
 
 def load_peaks():
@@ -199,6 +211,7 @@ def build_inputs(w, device):
 
 def bench_workload(w, args, rank, world, device, with_e2e):
     import torch
+    from tree_speculative_decoding_eagle_gb300.replicas import max_over_ranks
 
     dist = world > 1
     if dist:
@@ -282,10 +295,7 @@ def bench_workload(w, args, rank, world, device, with_e2e):
         torch.cuda.synchronize()
         stage_ms[name] = a.elapsed_time(b) / reps
 
-    if dist:
-        t = torch.tensor([elapsed_ms], device=device)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, device)   # the slowest replica sets the job's time
     ms_per_step = elapsed_ms / args.steps
     value = world * args.steps / (elapsed_ms / 1e3)
 
@@ -301,8 +311,12 @@ def bench_workload(w, args, rank, world, device, with_e2e):
 
 def bench_e2e(step, base, graph, dev_set, args, world, device):
     """Same step through the public API with host buffers: every step copies
-    its inputs from pinned host memory and reads its result back."""
+    its inputs from pinned host memory, calls TreeStep (one C-ABI call per
+    stage) and reads its result back.  `graph_value` replays the same calls
+    captured in a CUDA graph instead (how a serving loop would issue them)."""
     import torch
+    import torch.distributed as tdist
+    from tree_speculative_decoding_eagle_gb300.replicas import max_over_ranks
     host = {k: (v.cpu().pin_memory() if v is not None else None) for k, v in dev_set.items()}
     h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
     acc_h = torch.empty_like(step.accept_len, device="cpu").pin_memory()
@@ -310,24 +324,32 @@ def bench_e2e(step, base, graph, dev_set, args, world, device):
     d2h = acc_h.numel() * 4 + tok_h.numel() * 4
     stream = torch.cuda.current_stream()
 
-    def one():
+    def one(use_graph):
         for k, v in host.items():
             if v is not None:
                 dev_set[k].copy_(v, non_blocking=True)
-        graph.replay()
+        if use_graph:
+            graph.replay()
+        else:
+            step(**dev_set)
         acc_h.copy_(step.accept_len, non_blocking=True)
         tok_h.copy_(step.out_tokens, non_blocking=True)
         stream.synchronize()
 
-    for _ in range(max(3, args.warmup)):
-        one()
     steps = max(5, min(args.steps, 50))
-    t0 = time.perf_counter()
-    for _ in range(steps):
-        one()
-    dt = time.perf_counter() - t0
-    return {"value": world * steps / dt, "unit": "steps/s", "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "steps": steps}
+    rates = {}
+    for use_graph in (False, True):
+        for _ in range(max(3, args.warmup)):
+            one(use_graph)
+        if world > 1:
+            tdist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            one(use_graph)
+        dt = max_over_ranks(time.perf_counter() - t0, device)
+        rates[use_graph] = world * steps / dt
+    return {"value": rates[False], "unit": "steps/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": steps, "graph_value": rates[True]}
 
 
 def roofline(res, peaks, peak_src, workload_name):
@@ -486,6 +508,8 @@ def main(argv=None):
 
     peaks, peak_src = load_peaks()
     w = gen.WORKLOADS[args.workload]
+    if args.batch:
+        w = gen.scaled(w, B=args.batch)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = run_cpu_baseline(args.workload, args.cpu_seconds)
@@ -506,7 +530,7 @@ def main(argv=None):
             tdist.destroy_process_group()
         return
     step_gbs = res["step_bytes"] / (res["ms_per_step"] * 1e-3) / 1e9
-    n_launch = {"draft_topk": 1, "tree_build": 1, "tree_attn": 2, "verify": 2}
+    n_launch = launches_per_step(w)
     line = {
         "metric": "tree-spec steps/sec (build+attn+verify) at B=1 and B=64; HBM GB/s vs peak",
         "value": round(res["value"], 2), "unit": "steps/s", "n_gpus": world,
@@ -525,6 +549,7 @@ def main(argv=None):
         "cpu_baseline": cpu,
         "e2e": res["e2e"],
         "gpu_launches": args.steps * sum(n_launch.values()),
+        "launches_per_step": n_launch,
         "clocks": res["clocks"],
         "mean_accept_len": res["tau"],
         "also": also,
