@@ -16,12 +16,16 @@
 //     the ragged last prefix tile;
 //   * MMA warp (one elected thread): S_t = Q_t K^T (A = Q from shared
 //     memory) and O_t += P_t V (A = P from tensor memory), accumulators in
-//     tensor memory, completion via tcgen05.commit on mbarriers; S of the
-//     next tile is issued before P.V of the current one;
+//     tensor memory, completion via tcgen05.commit on mbarriers.  Each M-tile
+//     advances on its own events: as soon as its softmax has read S of tile
+//     j, S of tile j+1 is issued for it, then its P.V of tile j;
 //   * one softmax warpgroup per M-tile: reads its S rows from tensor memory
 //     (a max pass, then an exponent pass), writes P as packed bf16 pairs into
 //     tensor memory, keeps the row sum, and rescales its O rows in tensor
-//     memory only when the running maximum grows by more than 2^8.
+//     memory only when the running maximum grows by more than 2^8.  With two
+//     M-tiles the exponent passes take turns (a token passed through two
+//     mbarriers), so one M-tile's exponents overlap the other's MMAs and max
+//     pass instead of both competing for the same issue slots.
 // Tensor memory per M-tile: S (NK columns), P (NK/2), O (dh).
 // Every wait is bounded; a timeout raises EAGLE_ERR_TIMEOUT in the status
 // word and the CTA drains its copies and MMAs, frees tensor memory and exits.
@@ -53,7 +57,7 @@ struct TcShape {
   static constexpr int kTileBytes = kRegions * NK * 128;     // one K (or V) tile
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kBarOff = kQBytes + STAGES * kStageBytes;
-  static constexpr int kNumBars = 2 * STAGES + 4 * MT + 1;
+  static constexpr int kNumBars = 2 * STAGES + 4 * MT + 3;
   static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;  // + alignment slack
   static constexpr int kThreads = MT * 128 + 64;
   static constexpr int kColS = 0;                            // S_t at t*NK
@@ -84,6 +88,7 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
   uint64_t *p_full = s_free + MT;
   uint64_t *o_done = p_full + MT;
   uint64_t *teardown = o_done + MT;
+  uint64_t *turn = teardown + 1;  // exponent-pass token of M-tile 0 / 1
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Sh::kNumBars);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -128,6 +133,8 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
       mbar_init(&o_done[t], 1);
     }
     mbar_init(teardown, 1);
+    mbar_init(&turn[0], 4);
+    mbar_init(&turn[1], 4);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -197,33 +204,35 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(128, NK, false);
       constexpr uint32_t id_o = idesc_bf16(128, DH, true);
-      // S for tile j+1 is issued as soon as the softmax is done with tile j's
-      // S, so it overlaps that softmax's tail; P.V for tile j follows its P.
-      auto issue_s = [&](int j) -> bool {
-        const int st = j % STAGES;
-        if (!mbar_wait(&kv_full[st], (j / STAGES) & 1, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t kaddr = smem_u32(sKV + st * Sh::kStageBytes);
-        for (int t = 0; t < MT; ++t) {
-          if (j > 0 && !mbar_wait(&s_free[t], (j - 1) & 1, abort_flag)) return false;
-          tc_fence_after();
-          const uint32_t qaddr = smem_u32(sQ + t * Sh::kRegions * 16384);
+      auto issue_s = [&](int j, int t) {
+        const uint32_t kaddr = smem_u32(sKV + (j % STAGES) * Sh::kStageBytes);
+        const uint32_t qaddr = smem_u32(sQ + t * Sh::kRegions * 16384);
 #pragma unroll
-          for (int s = 0; s < DH / 16; ++s) {
-            const uint64_t ad = sdesc_sw128(qaddr + (s / 4) * 16384 + (s % 4) * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(kaddr + (s / 4) * (NK * 128) + (s % 4) * 32, 16, 1024);
-            mma_bf16_ss(tmem + Sh::kColS + t * NK, ad, bd, id_s, s > 0);
-          }
-          mma_commit(&s_full[t]);
+        for (int s = 0; s < DH / 16; ++s) {
+          const uint64_t ad = sdesc_sw128(qaddr + (s / 4) * 16384 + (s % 4) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(kaddr + (s / 4) * (NK * 128) + (s % 4) * 32, 16, 1024);
+          mma_bf16_ss(tmem + Sh::kColS + t * NK, ad, bd, id_s, s > 0);
         }
-        return true;
+        mma_commit(&s_full[t]);
       };
-      bool ok = T == 0 || issue_s(0);
+      bool ok = T == 0 || mbar_wait(&kv_full[0], 0, abort_flag);
+      if (ok && T > 0) {
+        tc_fence_after();
+        for (int t = 0; t < MT; ++t) issue_s(0, t);
+      }
+      // per tile j and M-tile t: S(j+1) as soon as the softmax has read S(j),
+      // then P(j).V once P(j) is in tensor memory
       for (int j = 0; j < T && ok; ++j) {
         const int st = j % STAGES;
-        if (j + 1 < T && !issue_s(j + 1)) break;
+        const bool next = j + 1 < T;
+        if (next && !mbar_wait(&kv_full[(j + 1) % STAGES], ((j + 1) / STAGES) & 1, abort_flag)) break;
         const uint32_t vaddr = smem_u32(sKV + st * Sh::kStageBytes) + Sh::kTileBytes;
         for (int t = 0; t < MT && ok; ++t) {
+          if (next) {
+            if (!mbar_wait(&s_free[t], j & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            issue_s(j + 1, t);
+          }
           if (!mbar_wait(&p_full[t], j & 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint32_t pcol = tmem + Sh::kColP + t * (NK / 2);
@@ -276,16 +285,15 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
 #pragma unroll
       for (int h = 0; h < NH; ++h) dense = dense && keep[h] == ~0ull;
       dense = __all_sync(0xffffffffu, dense);
-      // pass 1: masked maximum of the row's scores
-      float tmax = -INFINITY;
-#pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        float sv[64];
+      // scores of one 64-key half, masked keys at -inf
+      auto load_half = [&](int h, float (&sv)[64]) {
         tmem_ld64(tS + 64 * h, sv);
         if (!dense) {
 #pragma unroll
           for (int c = 0; c < 64; ++c) sv[c] = ((keep[h] >> c) & 1ull) ? sv[c] : -INFINITY;
         }
+      };
+      auto half_max = [](const float (&sv)[64]) {
         float mx[4] = {sv[0], sv[1], sv[2], sv[3]};
 #pragma unroll
         for (int c = 4; c < 64; c += 8) {
@@ -294,7 +302,22 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
           mx[2] = fmax3(mx[2], sv[c + 2], sv[c + 6]);
           mx[3] = fmax3(mx[3], sv[c + 3], sv[c + 7]);
         }
-        tmax = fmax3(tmax, fmax3(mx[0], mx[1], mx[2]), mx[3]);
+        return fmax3(fmax3(mx[0], mx[1], mx[2]), mx[3], -INFINITY);
+      };
+      // pass 1: masked maximum of the row's scores (a one-half tile keeps its
+      // scores in registers for pass 2)
+      float sv0[64];
+      float tmax = -INFINITY;
+      if constexpr (NH == 1) {
+        load_half(0, sv0);
+        tmax = half_max(sv0);
+      } else {
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          float sv[64];
+          load_half(h, sv);
+          tmax = fmaxf(tmax, half_max(sv));
+        }
       }
       tmax *= a.scale_log2;  // scale > 0
       const bool raise = tmax > m + 8.f;
@@ -305,34 +328,52 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
         if (!warp_wait(&o_done[t], (j - 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
       }
+      if constexpr (MT == 2) {  // wait for this M-tile's turn at the exponent pass
+        if ((t == 1 || j > 0) && !warp_wait(&turn[t], t == 1 ? (j & 1) : ((j - 1) & 1), abort_flag)) {
+          ok = false;
+          break;
+        }
+      }
       // pass 2: P = exp2(s*scale - base), packed bf16 pairs into tensor memory
       // (a row with no valid key yet has base -inf and only -inf scores: any
       // finite exponent base then gives 0)
       const float nb = base > -INFINITY ? -base : 0.f;
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        float sv[64];
-        tmem_ld64(tS + 64 * h, sv);
-        if (!dense) {
-#pragma unroll
-          for (int c = 0; c < 64; ++c) sv[c] = ((keep[h] >> c) & 1ull) ? sv[c] : -INFINITY;
-        }
+      const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2), nb2 = f2_pack(nb, nb);
+      uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
+      auto exp_half = [&](int h, const float (&sv)[64]) {
         float pk[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          const float p0v = ex2_approx(fmaf(sv[2 * c], a.scale_log2, nb));
-          const float p1v = ex2_approx(fmaf(sv[2 * c + 1], a.scale_log2, nb));
-          ps[c & 3] += p0v + p1v;
+          float t0, t1;
+          f2_unpack(f2_fma(f2_pack(sv[2 * c], sv[2 * c + 1]), sc2, nb2), t0, t1);
+          const float p0v = ex2_approx(t0), p1v = ex2_approx(t1);
+          if (c & 1) acc1 = f2_add(acc1, f2_pack(p0v, p1v));
+          else acc0 = f2_add(acc0, f2_pack(p0v, p1v));
           __nv_bfloat162 h2 = __floats2bfloat162_rn(p0v, p1v);
           pk[c] = *reinterpret_cast<const float *>(&h2);
         }
         tmem_st32(tP + 32 * h, pk);
+      };
+      if constexpr (NH == 1) {
+        exp_half(0, sv0);
+      } else {
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          float sv[64];
+          load_half(h, sv);
+          exp_half(h, sv);
+        }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[t]);  // S has been read
-      l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+      if (lane == 0) {
+        mbar_arrive(&s_free[t]);                           // S has been read
+        if constexpr (MT == 2) mbar_arrive(&turn[1 - t]);  // the other M-tile's turn
+      }
+      float q0, q1, q2, q3;
+      f2_unpack(acc0, q0, q1);
+      f2_unpack(acc1, q2, q3);
+      l = l * alpha + ((q0 + q1) + (q2 + q3));
       if (j > 0 && __any_sync(0xffffffffu, raise)) {
 #pragma unroll
         for (int c0 = 0; c0 < DH; c0 += 32) {
