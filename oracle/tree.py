@@ -28,6 +28,21 @@ Readings where the page leaves a point open:
 Because c <= 1, fl32(V * c) <= V, and a parent's gid is below its children's,
 every ancestor precedes its descendants in key order, so the top-m set is
 already closed and the closure step adds nothing; `build_tree` checks it.
+
+Ablation variants ([EAGLE-2] section "実験結果", ablation table: "without the
+global acceptance probability (confidence only)" and "without reranking"):
+  * confidence_only: a candidate is ranked by its own confidence c instead
+    of V, in the expansion and in the rerank.  Reading: c does not shrink
+    along a path, so the m best keys need not form a connected tree; the
+    rerank then grows the tree best-first, repeatedly adding the candidate
+    with the greatest key among those whose parent is already in the tree.
+    With V keys that is exactly the top-m set (ancestors outrank their
+    descendants), so the full method is the same procedure.
+  * rerank=False: the tree is the layers' selections E_1, E_2, ..., E_D in
+    depth order, each layer's k greatest keys (E_D chosen the same way,
+    although it is never expanded), truncated to m nodes; m <= D*k.
+  * node score: the value the node was ranked by (V, or c when
+    confidence_only).
 """
 import numpy as np
 
@@ -47,11 +62,12 @@ class Candidates:
         self.score = [np.float32(1.0)]
         self.row = [0]          # draft row slot d*k + j if expanded, else -1
 
-    def add(self, parent, token, conf, depth):
+    def add(self, parent, token, conf, depth, confidence_only=False):
         self.parent.append(int(parent))
         self.token.append(int(token))
         self.depth.append(int(depth))
-        self.score.append(fl32_mul(self.score[parent], conf))
+        self.score.append(np.float32(conf) if confidence_only
+                          else fl32_mul(self.score[parent], conf))
         self.row.append(-1)
         return len(self.parent) - 1
 
@@ -63,12 +79,14 @@ class Candidates:
         return len(self.parent)
 
 
-def build_tree(tok, conf, m, root_token=-1, return_candidates=False):
+def build_tree(tok, conf, m, root_token=-1, return_candidates=False,
+               confidence_only=False, rerank=True):
     """Build one sequence's draft tree.
 
     tok  int [D, k, k]   top-k token ids of each used draft row
     conf fp32 [D, k, k]  their confidences (rows [0, 1..k-1] unused)
     m    number of draft tokens to keep
+    confidence_only, rerank: the ablation variants (module docstring)
 
     Returns a dict of arrays over the m+1 output nodes (root = node 0):
       tok, parent (output index, root -1), depth, score (fp32 V), src (gid),
@@ -81,19 +99,35 @@ def build_tree(tok, conf, m, root_token=-1, return_candidates=False):
     assert k == k2
     C = Candidates(root_token)
 
-    layer = [C.add(0, tok[0, 0, r], conf[0, 0, r], 1) for r in range(k)]
-    for d in range(1, D):
+    layer = [C.add(0, tok[0, 0, r], conf[0, 0, r], 1, confidence_only) for r in range(k)]
+    selections = []                      # E_1, E_2, ...: each layer's k best
+    for d in range(1, D + 1):
         expanded = sorted(layer, key=C.key)[:k]
+        selections.append(expanded)
+        if d == D:
+            break
         nxt = []
         for j, p in enumerate(expanded):
             C.row[p] = d * k + j
             for r in range(k):
-                nxt.append(C.add(p, tok[d, j, r], conf[d, j, r], d + 1))
+                nxt.append(C.add(p, tok[d, j, r], conf[d, j, r], d + 1, confidence_only))
         layer = nxt
 
     n_cand = len(C) - 1
     assert 1 <= m <= n_cand, "m must not exceed the number of candidates"
-    kept = sorted(range(1, len(C)), key=C.key)[:m]
+    if not rerank:
+        assert m <= D * k, "without rerank the tree holds at most D*k nodes"
+        kept = [g for sel in selections for g in sel][:m]
+    elif confidence_only:
+        kept = []
+        inside = {0}
+        for _ in range(m):
+            open_ = [g for g in range(1, len(C)) if g not in inside and C.parent[g] in inside]
+            best = min(open_, key=C.key)
+            kept.append(best)
+            inside.add(best)
+    else:
+        kept = sorted(range(1, len(C)), key=C.key)[:m]
 
     chosen = set(kept)
     added = []
@@ -105,7 +139,10 @@ def build_tree(tok, conf, m, root_token=-1, return_candidates=False):
                 added.append(a)
             a = C.parent[a]
 
-    order = [0] + sorted(chosen, key=C.key)
+    if rerank and not confidence_only:
+        order = [0] + sorted(chosen, key=C.key)
+    else:
+        order = [0] + kept           # selection order: parents come first
     index_of = {g: i for i, g in enumerate(order)}
     out = dict(
         tok=np.array([C.token[g] for g in order], dtype=np.int64),
@@ -121,7 +158,7 @@ def build_tree(tok, conf, m, root_token=-1, return_candidates=False):
     return out
 
 
-def build_trees(tok, conf, m, root_tokens=None):
+def build_trees(tok, conf, m, root_tokens=None, confidence_only=False, rerank=True):
     """Batch version: tok [B, D, k, k], conf [B, D, k, k] -> stacked arrays.
 
     Requires the closure to add nothing (true whenever 0 <= c <= 1), so every
@@ -129,7 +166,8 @@ def build_trees(tok, conf, m, root_tokens=None):
     """
     B = tok.shape[0]
     outs = [build_tree(tok[b], conf[b], m,
-                       -1 if root_tokens is None else root_tokens[b])
+                       -1 if root_tokens is None else root_tokens[b],
+                       confidence_only=confidence_only, rerank=rerank)
             for b in range(B)]
     for o in outs:
         assert not o["closure_added"], "closure added nodes (a confidence > 1?)"
