@@ -167,6 +167,35 @@ int eagle_tree_build(const int32_t *tok, const float *conf, int B, int D, int k,
                      uint64_t *mask, int32_t *status, eagle_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Stage 2, ablation variants of the tree build.
+ * [EAGLE-2] section "実験結果", ablation table: the method without the global
+ * acceptance probability ("confidence only") and without reranking.  Same
+ * arguments, outputs and limits as eagle_tree_build, plus `flags`, a bitwise
+ * OR of:
+ *   EAGLE_TREE_CONFIDENCE_ONLY  rank a candidate by its own confidence c
+ *       instead of V (node_score then holds c).  The expansion takes each
+ *       layer's k greatest keys as before; the rerank grows the tree
+ *       best-first, repeatedly adding the greatest key whose parent is
+ *       already in the tree (with V keys this is exactly the top-m set), so
+ *       node order is the order of selection and every parent precedes its
+ *       children.
+ *   EAGLE_TREE_NO_RERANK  no rerank: the tree is the layers' selections
+ *       E_1, E_2, ..., E_D (each layer's k greatest keys; E_D chosen the
+ *       same way although never expanded), in depth order and rank order
+ *       within a depth, truncated to m nodes.  Requires m <= D*k.
+ * flags = 0 is eagle_tree_build.  Other bits: EAGLE_ERR_INVALID.
+ * ------------------------------------------------------------------------ */
+#define EAGLE_TREE_CONFIDENCE_ONLY 1
+#define EAGLE_TREE_NO_RERANK 2
+int eagle_tree_build_variant(const int32_t *tok, const float *conf, int B, int D,
+                             int k, int m, int flags, const int32_t *root_tok,
+                             int32_t *node_tok, int32_t *node_parent,
+                             int32_t *node_depth, float *node_score,
+                             int32_t *node_src, int32_t *node_row,
+                             uint64_t *mask, int32_t *status,
+                             eagle_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Ancestor-only attention mask.
  * [EAGLE-2] section "注意マスクの調整": each token attends only to its
  * ancestors.  Bit (j % 64) of word j / 64 of row i is set iff j == i or j is

@@ -63,6 +63,12 @@ def test_invalid_arguments_are_rejected_on_the_host(lib):
     assert lib.eagle_tree_build(*args) == -1
     args[3], args[4], args[5] = 6, 32, 10       # 32 + 5*1024 > 4095
     assert lib.eagle_tree_build(*args) == -1
+    # tree_build_variant: unknown flag bits, no-rerank with m beyond D*k
+    va = [fake, fake, 1, 3, 2, 5, 4, NULL, fake, fake, NULL, NULL, NULL, NULL, NULL, NULL, NULL]
+    assert lib.eagle_tree_build_variant(*va) == -1
+    va[6] = 2                                   # D*k = 6 >= m = 5: accepted until launch, so use m = 7
+    va[5] = 7
+    assert lib.eagle_tree_build_variant(*va) == -1
     # tree_mask: n out of range
     assert lib.eagle_tree_mask(fake, 1, 0, fake, NULL) == -1
     assert lib.eagle_tree_mask(fake, 1, 5000, fake, NULL) == -1

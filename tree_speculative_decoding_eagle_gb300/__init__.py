@@ -7,7 +7,8 @@ computation runs in the library's kernels.  There is no fallback: if the
 library is missing or a call reports an error, an exception is raised.
 
     draft_topk  -> eagle_draft_topk   (softmax statistics + top-k per draft row)
-    tree_build  -> eagle_tree_build   (global scores, expansion, rerank, mask)
+    tree_build  -> eagle_tree_build   (global scores, expansion, rerank, mask;
+                   eagle_tree_build_variant for the ablation flags)
     tree_mask   -> eagle_tree_mask    (ancestor-only attention mask)
     tree_attn   -> eagle_tree_attn    (tree-masked attention over the KV prefix)
     verify      -> eagle_verify       (greedy / speculative-sampling walk)
@@ -22,11 +23,12 @@ LIB_PATH = os.path.join(_PKG, "_build", "libeagle.so")
 
 F32, BF16 = 0, 1
 GREEDY, SAMPLE = 0, 1
+TREE_CONFIDENCE_ONLY, TREE_NO_RERANK = 1, 2
 
 EXPORTED = (
     "eagle_status_string", "eagle_version",
     "eagle_draft_topk_workspace_size", "eagle_draft_topk", "eagle_draft_topk_noalloc",
-    "eagle_tree_build", "eagle_tree_mask",
+    "eagle_tree_build", "eagle_tree_build_variant", "eagle_tree_mask",
     "eagle_tree_attn_workspace_size", "eagle_tree_attn",
     "eagle_verify_workspace_size", "eagle_verify",
 )
@@ -54,6 +56,7 @@ def load_library(path=LIB_PATH):
         "eagle_draft_topk": (I, [P, I, I, I, I, I, I64, P, P, P, P, P, SZ, P]),
         "eagle_draft_topk_noalloc": (I, [P, I, I, I, I, I, I64, P, P, P, P, P]),
         "eagle_tree_build": (I, [P, P, I, I, I, I, P, P, P, P, P, P, P, P, P, P]),
+        "eagle_tree_build_variant": (I, [P, P, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P]),
         "eagle_tree_mask": (I, [P, I, I, P, P]),
         "eagle_tree_attn_workspace_size": (SZ, [I, I, I, I, I, I, I]),
         "eagle_tree_attn": (I, [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, P, P, P, SZ, P]),
@@ -157,8 +160,11 @@ def draft_topk_noalloc(logits, k, tok=None, conf=None, stats=None, status=None, 
     return tok, conf, stats
 
 
-def tree_build(tok, conf, m, root_tok=None, with_mask=True, out=None, status=None, stream=None):
-    """tok/conf [B, D, k, k] -> dict of node arrays [B, m+1] (+ mask [B, m+1, W])."""
+def tree_build(tok, conf, m, root_tok=None, with_mask=True, out=None, status=None, stream=None, flags=0):
+    """tok/conf [B, D, k, k] -> dict of node arrays [B, m+1] (+ mask [B, m+1, W]).
+
+    flags: 0 for the method, or TREE_CONFIDENCE_ONLY | TREE_NO_RERANK for the
+    ablation variants (eagle_tree_build_variant)."""
     lib = load_library()
     _cuda(tok, "tok")
     B, D, k, _ = tok.shape
@@ -174,10 +180,17 @@ def tree_build(tok, conf, m, root_tok=None, with_mask=True, out=None, status=Non
     o.setdefault("row", torch.empty((B, n), dtype=torch.int32, device=dev))
     if with_mask:
         o.setdefault("mask", torch.empty((B, n, W), dtype=torch.int64, device=dev))
-    _check(lib.eagle_tree_build(_ptr(tok), _ptr(conf), B, D, k, m, _ptr(root_tok), _ptr(o["tok"]),
-                                _ptr(o["parent"]), _ptr(o["depth"]), _ptr(o["score"]),
-                                _ptr(o["src"]), _ptr(o["row"]), _ptr(o.get("mask")),
-                                _ptr(status), _stream(stream)), "eagle_tree_build")
+    if flags:
+        _check(lib.eagle_tree_build_variant(_ptr(tok), _ptr(conf), B, D, k, m, int(flags), _ptr(root_tok),
+                                            _ptr(o["tok"]), _ptr(o["parent"]), _ptr(o["depth"]),
+                                            _ptr(o["score"]), _ptr(o["src"]), _ptr(o["row"]),
+                                            _ptr(o.get("mask")), _ptr(status), _stream(stream)),
+               "eagle_tree_build_variant")
+    else:
+        _check(lib.eagle_tree_build(_ptr(tok), _ptr(conf), B, D, k, m, _ptr(root_tok), _ptr(o["tok"]),
+                                    _ptr(o["parent"]), _ptr(o["depth"]), _ptr(o["score"]),
+                                    _ptr(o["src"]), _ptr(o["row"]), _ptr(o.get("mask")),
+                                    _ptr(status), _stream(stream)), "eagle_tree_build")
     return o
 
 

@@ -12,7 +12,7 @@ cudaError_t launch_draft_topk(const void *logits, int dtype, int B, int D, int k
                               int32_t *tok, float *conf, float *stats, void *ws, int32_t *status,
                               int num_sms, cudaStream_t st);
 // tree_build.cu
-cudaError_t launch_tree_build(const int32_t *tok, const float *conf, int B, int D, int k, int m,
+cudaError_t launch_tree_build(const int32_t *tok, const float *conf, int B, int D, int k, int m, int flags,
                               const int32_t *root_tok, int32_t *node_tok, int32_t *node_parent,
                               int32_t *node_depth, float *node_score, int32_t *node_src,
                               int32_t *node_row, uint64_t *mask, int32_t *status, cudaStream_t st);
@@ -100,18 +100,28 @@ int eagle_draft_topk(const void *logits, int dtype, int B, int D, int k, int V, 
                                      status, sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int eagle_tree_build_variant(const int32_t *tok, const float *conf, int B, int D, int k, int m, int flags,
+                             const int32_t *root_tok, int32_t *node_tok, int32_t *node_parent,
+                             int32_t *node_depth, float *node_score, int32_t *node_src, int32_t *node_row,
+                             uint64_t *mask, int32_t *status, eagle_stream_t stream) {
+  if (!tok || !conf || !node_tok || !node_parent) return EAGLE_ERR_INVALID;
+  if (B < 1 || D < 1 || k < 1 || k > 32 || m < 1) return EAGLE_ERR_INVALID;
+  if (flags & ~(EAGLE_TREE_CONFIDENCE_ONLY | EAGLE_TREE_NO_RERANK)) return EAGLE_ERR_INVALID;
+  const int64_t NC = k + static_cast<int64_t>(D - 1) * k * k;
+  if (NC > 4095 || m > NC) return EAGLE_ERR_INVALID;
+  if ((flags & EAGLE_TREE_NO_RERANK) && m > static_cast<int64_t>(D) * k) return EAGLE_ERR_INVALID;
+  if (tree_smem_bytes(D, k, m) > 227 * 1024) return EAGLE_ERR_UNSUPPORTED;  // one CTA's shared memory
+  return from_cuda(launch_tree_build(tok, conf, B, D, k, m, flags, root_tok, node_tok, node_parent,
+                                     node_depth, node_score, node_src, node_row, mask, status,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int eagle_tree_build(const int32_t *tok, const float *conf, int B, int D, int k, int m,
                      const int32_t *root_tok, int32_t *node_tok, int32_t *node_parent,
                      int32_t *node_depth, float *node_score, int32_t *node_src, int32_t *node_row,
                      uint64_t *mask, int32_t *status, eagle_stream_t stream) {
-  if (!tok || !conf || !node_tok || !node_parent) return EAGLE_ERR_INVALID;
-  if (B < 1 || D < 1 || k < 1 || k > 32 || m < 1) return EAGLE_ERR_INVALID;
-  const int64_t NC = k + static_cast<int64_t>(D - 1) * k * k;
-  if (NC > 4095 || m > NC) return EAGLE_ERR_INVALID;
-  if (tree_smem_bytes(D, k, m) > 227 * 1024) return EAGLE_ERR_UNSUPPORTED;  // one CTA's shared memory
-  return from_cuda(launch_tree_build(tok, conf, B, D, k, m, root_tok, node_tok, node_parent,
-                                     node_depth, node_score, node_src, node_row, mask, status,
-                                     reinterpret_cast<cudaStream_t>(stream)));
+  return eagle_tree_build_variant(tok, conf, B, D, k, m, 0, root_tok, node_tok, node_parent, node_depth,
+                                  node_score, node_src, node_row, mask, status, stream);
 }
 
 int eagle_tree_mask(const int32_t *node_parent, int B, int n, uint64_t *mask, eagle_stream_t stream) {

@@ -10,9 +10,17 @@
 // One CTA per sequence, everything in shared memory.  A candidate is a
 // 64-bit key  bits(V):32 | (4095 - parent gid):12 | (2^20 - 1 - token):20,
 // so unsigned order is the rank order (V desc, parent gid asc, token asc)
-// and keys are unique.  Ranks are obtained by counting larger keys (8 lanes
+// and keys are unique.  Ranks are obtained by counting larger keys (4 lanes
 // per item, shuffle-reduced).  The running top-m list is merged with each
 // new layer by rank arithmetic, so the whole candidate set is never sorted.
+//
+// Ablation variants ([EAGLE-2] section "実験結果", ablation table), chosen by
+// flags: EAGLE_TREE_CONFIDENCE_ONLY ranks a candidate by its own confidence
+// c instead of V (expansion and rerank; the rerank then grows the tree
+// best-first: the greatest key whose parent is already in the tree, which
+// with V keys is the same top-m set); EAGLE_TREE_NO_RERANK keeps the
+// layers' selections E_1, E_2, ... (each layer's k best keys) in depth
+// order, truncated to m nodes.
 #include "common.cuh"
 
 namespace eagle {
@@ -32,7 +40,7 @@ __device__ __forceinline__ int tkey_token(uint64_t k) { return 0xFFFFF - static_
 struct TreeArgs {
   const int32_t *tok;
   const float *conf;
-  int B, D, k, m, NC;
+  int B, D, k, m, NC, flags;
   const int32_t *root_tok;
   int32_t *node_tok, *node_parent, *node_depth, *node_src, *node_row;
   float *node_score;
@@ -98,9 +106,13 @@ __global__ void __launch_bounds__(kTreeThreads) tree_build_kernel(TreeArgs a) {
   int *s_out = s_row + (NC + 1);                                 // [NC+1] gid -> node
   int *s_par = s_out + (NC + 1);                                 // [n]
   int *s_E = s_par + n;                                          // [k]
-  int *s_tok = s_E + k;                                          // [R*k] used rows
+  int *s_sel = s_E + k;                                          // [m] gids in output order
+  int *s_tok = s_sel + m;                                        // [R*k] used rows
   float *s_conf = reinterpret_cast<float *>(s_tok + (1 + (D - 1) * k) * k);
   __shared__ int s_bad;
+  const bool conf_only = (a.flags & EAGLE_TREE_CONFIDENCE_ONLY) != 0;
+  const bool rerank = (a.flags & EAGLE_TREE_NO_RERANK) == 0;
+  const bool full = rerank && !conf_only;  // top-m by incremental merge
 
   const int32_t *tok = a.tok + static_cast<int64_t>(b) * D * kk;
   const float *conf = a.conf + static_cast<int64_t>(b) * D * kk;
@@ -143,10 +155,13 @@ __global__ void __launch_bounds__(kTreeThreads) tree_build_kernel(TreeArgs a) {
     const uint64_t *layer = s_key + base;
     uint64_t *L = s_L + cur * m;
     int *Lg = s_Lg + cur * m;
-    // ranks within the layer, layer vs list, list vs layer
+    // ranks within the layer; in the full method also layer vs list and
+    // list vs layer for the running top-m merge
     count_greater(layer, nl, layer, nl, s_cnt);
-    count_greater(layer, nl, L, nL, s_cnt + kk);
-    count_greater(L, nL, layer, nl, s_cnt + 2 * kk);
+    if (full) {
+      count_greater(layer, nl, L, nL, s_cnt + kk);
+      count_greater(L, nL, layer, nl, s_cnt + 2 * kk);
+    }
     __syncthreads();
     uint64_t *L2 = s_L + (cur ^ 1) * m;
     int *Lg2 = s_Lg + (cur ^ 1) * m;
@@ -156,21 +171,27 @@ __global__ void __launch_bounds__(kTreeThreads) tree_build_kernel(TreeArgs a) {
         s_E[rank] = base + q;
         s_row[base + q] = d * k + rank;
       }
-      const int pos = rank + s_cnt[kk + q];
-      if (pos < m) {
-        L2[pos] = layer[q];
-        Lg2[pos] = base + q;
+      if (full) {
+        const int pos = rank + s_cnt[kk + q];
+        if (pos < m) {
+          L2[pos] = layer[q];
+          Lg2[pos] = base + q;
+        }
+      } else if (!rerank && rank < k && (d - 1) * k + rank < m) {
+        s_sel[(d - 1) * k + rank] = base + q;
       }
     }
-    for (int q = tid; q < nL; q += blockDim.x) {
-      const int pos = q + s_cnt[2 * kk + q];
-      if (pos < m) {
-        L2[pos] = L[q];
-        Lg2[pos] = Lg[q];
+    if (full) {
+      for (int q = tid; q < nL; q += blockDim.x) {
+        const int pos = q + s_cnt[2 * kk + q];
+        if (pos < m) {
+          L2[pos] = L[q];
+          Lg2[pos] = Lg[q];
+        }
       }
+      nL = min(m, nL + nl);
+      cur ^= 1;
     }
-    nL = min(m, nL + nl);
-    cur ^= 1;
     if (d == D) break;
     __syncthreads();
     // children of the expanded nodes: row [d, j] for E[j]
@@ -179,16 +200,54 @@ __global__ void __launch_bounds__(kTreeThreads) tree_build_kernel(TreeArgs a) {
       const int j = q / k, r = q % k;
       const int p = s_E[j];
       const int slot = (1 + (d - 1) * k + j) * k + r;
-      const float v = __fadd_rn(__fmul_rn(tkey_score(s_key[p]), s_conf[slot]), 0.0f);
+      const float v = conf_only ? s_conf[slot] : __fadd_rn(__fmul_rn(tkey_score(s_key[p]), s_conf[slot]), 0.0f);
       s_key[nbase + q] = tree_key(v, p, s_tok[slot]);
     }
   }
   __syncthreads();
 
+  // ---- selection in output order ----------------------------------------
+  if (full) {
+    const int *Lg = s_Lg + cur * m;
+    for (int q = tid; q < m; q += blockDim.x) s_sel[q] = Lg[q];
+  } else if (rerank && (tid >> 5) == 0) {
+    // confidence only: best-first growth by one warp, m picks of the
+    // greatest key whose parent is already in the tree (s_out >= 0)
+    const int lane = tid & 31;
+    for (int pick = 0; pick < m; ++pick) {
+      uint64_t best = 0;
+      int bg = -1;
+      for (int g = 1 + lane; g <= NC; g += 32) {
+        const uint64_t key = s_key[g];
+        if (s_out[g] < 0 && s_out[tkey_parent(key)] >= 0 && (bg < 0 || key > best)) {
+          best = key;
+          bg = g;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const uint64_t ob = shfl_xor_u64(best, o);
+        const int og = __shfl_xor_sync(0xffffffffu, bg, o);
+        if (og >= 0 && (bg < 0 || ob > best)) {
+          best = ob;
+          bg = og;
+        }
+      }
+      if (bg < 0) {  // nothing left to add (cannot happen for m <= candidates)
+        if (lane == 0) s_bad = 1;
+        break;
+      }
+      if (lane == 0) {
+        s_out[bg] = pick + 1;
+        s_sel[pick] = bg;
+      }
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+
   // ---- outputs ---------------------------------------------------------
-  const uint64_t *L = s_L + cur * m;
-  const int *Lg = s_Lg + cur * m;
-  for (int q = tid; q < m; q += blockDim.x) s_out[Lg[q]] = q + 1;
+  for (int q = tid; q < m; q += blockDim.x) s_out[s_sel[q]] = q + 1;
   __syncthreads();
   const int64_t ob = static_cast<int64_t>(b) * n;
   for (int i = tid; i < n; i += blockDim.x) {
@@ -198,8 +257,8 @@ __global__ void __launch_bounds__(kTreeThreads) tree_build_kernel(TreeArgs a) {
       t = a.root_tok ? a.root_tok[b] : -1;
       par = -1; dep = 0; src = 0; row = 0; sc = 1.0f;
     } else {
-      const uint64_t key = L[i - 1];
-      src = Lg[i - 1];
+      src = s_sel[i - 1];
+      const uint64_t key = s_key[src];
       t = tkey_token(key);
       sc = tkey_score(key);
       par = s_out[tkey_parent(key)];
@@ -251,17 +310,18 @@ size_t tree_smem_bytes(int D, int k, int m) {
                + sizeof(int) * (2 * kk + m)           // s_cnt
                + sizeof(int) * 2 * (NC + 1)           // s_row, s_out
                + sizeof(int) * n + sizeof(int) * k    // s_par, s_E
+               + sizeof(int) * m                      // s_sel
                + 8 * static_cast<size_t>(1 + (D - 1) * k) * k;  // s_tok, s_conf
   return (bytes + 15) / 16 * 16;
 }
 
-cudaError_t launch_tree_build(const int32_t *tok, const float *conf, int B, int D, int k, int m,
+cudaError_t launch_tree_build(const int32_t *tok, const float *conf, int B, int D, int k, int m, int flags,
                               const int32_t *root_tok, int32_t *node_tok, int32_t *node_parent,
                               int32_t *node_depth, float *node_score, int32_t *node_src,
                               int32_t *node_row, uint64_t *mask, int32_t *status, cudaStream_t st) {
   TreeArgs a;
   a.tok = tok; a.conf = conf;
-  a.B = B; a.D = D; a.k = k; a.m = m;
+  a.B = B; a.D = D; a.k = k; a.m = m; a.flags = flags;
   a.NC = k + (D - 1) * k * k;
   a.root_tok = root_tok;
   a.node_tok = node_tok; a.node_parent = node_parent; a.node_depth = node_depth;
