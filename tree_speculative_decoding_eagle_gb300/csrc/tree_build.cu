@@ -48,24 +48,17 @@ struct TreeArgs {
   int32_t *status;
 };
 
-// Count, for each of n_items items, how many keys of `set` exceed the item's
-// key; 4 lanes per item.  Must be called by the whole block.
-__device__ __forceinline__ void count_greater(const uint64_t *item_keys, int n_items,
-                                              const uint64_t *set, int n_set, int *out) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nwarps = blockDim.x >> 5;
-  for (int base = warp * 8; base < n_items; base += nwarps * 8) {
-    const int it = base + (lane >> 2);
-    const int sub = lane & 3;
-    int cnt = 0;
-    if (it < n_items) {
-      const uint64_t me = item_keys[it];
-      for (int q = sub; q < n_set; q += 4) cnt += set[q] > me;
-    }
-    cnt += __shfl_xor_sync(0xffffffffu, cnt, 1);
-    cnt += __shfl_xor_sync(0xffffffffu, cnt, 2);
-    if (it < n_items && sub == 0) out[it] = cnt;
+// How many of the n keys of `set` exceed `me`.  Meant for a warp whose
+// lanes rank different items against the same set: every load is then a
+// shared-memory broadcast, eight in flight.
+__device__ __forceinline__ int count_greater(uint64_t me, const uint64_t *set, int n) {
+  int c = 0, q = 0;
+  for (; q + 8 <= n; q += 8) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) c += set[q + e] > me;
   }
+  for (; q < n; ++q) c += set[q] > me;
+  return c;
 }
 
 __device__ __forceinline__ int depth_of_gid(int g, int k) {
@@ -96,19 +89,19 @@ __global__ void __launch_bounds__(kTreeThreads) tree_build_kernel(TreeArgs a) {
   const int k = a.k, m = a.m, NC = a.NC, D = a.D;
   const int kk = k * k;
   const int n = m + 1;
+  const int R = 1 + (D - 1) * k;  // used draft rows
 
   // shared layout
-  uint64_t *s_key = reinterpret_cast<uint64_t *>(smem);        // [NC+1]
-  uint64_t *s_L = s_key + (NC + 1);                              // [2][m] keys
-  int *s_Lg = reinterpret_cast<int *>(s_L + 2 * m);              // [2][m] gids
-  int *s_cnt = s_Lg + 2 * m;                                     // [2*kk + m]
-  int *s_row = s_cnt + (2 * kk + m);                             // [NC+1]
-  int *s_out = s_row + (NC + 1);                                 // [NC+1] gid -> node
-  int *s_par = s_out + (NC + 1);                                 // [n]
-  int *s_E = s_par + n;                                          // [k]
-  int *s_sel = s_E + k;                                          // [m] gids in output order
-  int *s_tok = s_sel + m;                                        // [R*k] used rows
-  float *s_conf = reinterpret_cast<float *>(s_tok + (1 + (D - 1) * k) * k);
+  uint64_t *s_key = reinterpret_cast<uint64_t *>(smem);        // [NC+1] every candidate's key
+  uint64_t *s_L = s_key + (NC + 1);                              // [2][m] running top-m keys
+  int *s_Lg = reinterpret_cast<int *>(s_L + 2 * m);              // [2][m] their gids
+  int *s_cnt = s_Lg + 2 * m;                                     // [2*kk + m] ranks
+  int *s_row = s_cnt + (2 * kk + m);                             // [NC+1] gid -> draft row slot
+  int *s_out = s_row + (NC + 1);                                 // [NC+1] gid -> output node
+  int *s_sel = s_out + (NC + 1);                                 // [m] gids in output order
+  int *s_E = s_sel + m;                                          // [k] expanded gids by rank
+  int *s_tok = s_E + k;                                          // [R*k] used rows
+  float *s_conf = reinterpret_cast<float *>(s_tok + R * k);
   __shared__ int s_bad;
   const bool conf_only = (a.flags & EAGLE_TREE_CONFIDENCE_ONLY) != 0;
   const bool rerank = (a.flags & EAGLE_TREE_NO_RERANK) == 0;
@@ -119,13 +112,12 @@ __global__ void __launch_bounds__(kTreeThreads) tree_build_kernel(TreeArgs a) {
 
   if (tid == 0) s_bad = 0;
   for (int g = tid; g <= NC; g += blockDim.x) {
-    s_row[g] = -1;
-    s_out[g] = -1;
+    s_row[g] = g == 0 ? 0 : -1;
+    s_out[g] = g == 0 ? 0 : -1;
   }
   // used draft rows (slot 0 = row [0,0], slot 1+(d-1)k+j = row [d,j]) in one
   // coalesced pass; tokens and confidences outside the domain are flagged and
   // tokens clamped so the key fields stay in range
-  const int R = 1 + (D - 1) * k;
   for (int idx = tid; idx < R * k; idx += blockDim.x) {
     const int slot = idx / k, rr = idx % k;
     const int gi = slot == 0 ? rr : ((1 + (slot - 1) / k) * k + (slot - 1) % k) * k + rr;
@@ -137,51 +129,60 @@ __global__ void __launch_bounds__(kTreeThreads) tree_build_kernel(TreeArgs a) {
     s_conf[idx] = c;
   }
   __syncthreads();
-  if (tid == 0) {
-    s_row[0] = 0;
-    s_out[0] = 0;
-  }
 
-  // depth-1 layer: the root row's tokens
-  for (int r = tid; r < k; r += blockDim.x) {
-    const float c = __fadd_rn(__fmul_rn(1.0f, s_conf[r]), 0.0f);
-    s_key[1 + r] = tree_key(c, 0, s_tok[r]);
-  }
+  // depth-1 layer: the root row's tokens (V = fl32(1 * c) = c)
+  for (int r = tid; r < k; r += blockDim.x) s_key[1 + r] = tree_key(s_conf[r], 0, s_tok[r]);
   int nL = 0, cur = 0;
   for (int d = 1; d <= D; ++d) {
     __syncthreads();
     const int base = layer_base(d, k);
     const int nl = d == 1 ? k : kk;
     const uint64_t *layer = s_key + base;
-    uint64_t *L = s_L + cur * m;
-    int *Lg = s_Lg + cur * m;
-    // ranks within the layer; in the full method also layer vs list and
-    // list vs layer for the running top-m merge
-    count_greater(layer, nl, layer, nl, s_cnt);
-    if (full) {
-      count_greater(layer, nl, L, nL, s_cnt + kk);
-      count_greater(L, nL, layer, nl, s_cnt + 2 * kk);
+    const uint64_t *L = s_L + cur * m;
+    const int *Lg = s_Lg + cur * m;
+    // phase A, one thread per ranked item, jobs padded to whole warps: the
+    // rank of each layer key within the layer (its thread then records the
+    // expansion: draft row [d, rank] for rank < k, or the no-rerank slot);
+    // in the full method also each layer key against the running top-m list
+    // and each list key against the layer, for the merge
+    {
+      const int p0 = (nl + 31) & ~31, p1 = full ? p0 : 0, p2 = full ? ((nL + 31) & ~31) : 0;
+      for (int t = tid; t < p0 + p1 + p2; t += blockDim.x) {
+        if (t < p0) {
+          if (t < nl) {
+            const int r = count_greater(layer[t], layer, nl);
+            s_cnt[t] = r;
+            if (r < k) {
+              const int g = base + t;
+              if (d < D) {
+                s_E[r] = g;
+                s_row[g] = d * k + r;
+              }
+              if (!rerank && (d - 1) * k + r < m) s_sel[(d - 1) * k + r] = g;
+            }
+          }
+        } else if (t < p0 + p1) {
+          const int it = t - p0;
+          if (it < nl) s_cnt[kk + it] = count_greater(layer[it], L, nL);
+        } else {
+          const int it = t - p0 - p1;
+          if (it < nL) s_cnt[2 * kk + it] = count_greater(L[it], layer, nl);
+        }
+      }
     }
     __syncthreads();
-    uint64_t *L2 = s_L + (cur ^ 1) * m;
-    int *Lg2 = s_Lg + (cur ^ 1) * m;
-    for (int q = tid; q < nl; q += blockDim.x) {
-      const int rank = s_cnt[q];
-      if (d < D && rank < k) {
-        s_E[rank] = base + q;
-        s_row[base + q] = d * k + rank;
-      }
-      if (full) {
-        const int pos = rank + s_cnt[kk + q];
+    // phase B: the merge into the other top-m buffer, and the children of
+    // the expanded nodes (row [d, j] for E[j]) as the next layer
+    if (full) {
+      uint64_t *L2 = s_L + (cur ^ 1) * m;
+      int *Lg2 = s_Lg + (cur ^ 1) * m;
+      for (int q = tid; q < nl; q += blockDim.x) {
+        const int pos = s_cnt[q] + s_cnt[kk + q];
         if (pos < m) {
           L2[pos] = layer[q];
           Lg2[pos] = base + q;
         }
-      } else if (!rerank && rank < k && (d - 1) * k + rank < m) {
-        s_sel[(d - 1) * k + rank] = base + q;
       }
-    }
-    if (full) {
       for (int q = tid; q < nL; q += blockDim.x) {
         const int pos = q + s_cnt[2 * kk + q];
         if (pos < m) {
@@ -192,32 +193,33 @@ __global__ void __launch_bounds__(kTreeThreads) tree_build_kernel(TreeArgs a) {
       nL = min(m, nL + nl);
       cur ^= 1;
     }
-    if (d == D) break;
-    __syncthreads();
-    // children of the expanded nodes: row [d, j] for E[j]
-    const int nbase = layer_base(d + 1, k);
-    for (int q = tid; q < kk; q += blockDim.x) {
-      const int j = q / k, r = q % k;
-      const int p = s_E[j];
-      const int slot = (1 + (d - 1) * k + j) * k + r;
-      const float v = conf_only ? s_conf[slot] : __fadd_rn(__fmul_rn(tkey_score(s_key[p]), s_conf[slot]), 0.0f);
-      s_key[nbase + q] = tree_key(v, p, s_tok[slot]);
+    if (d < D) {
+      const int nbase = layer_base(d + 1, k);
+      for (int q = tid; q < kk; q += blockDim.x) {
+        const int j = q / k, r = q % k;
+        const int p = s_E[j];
+        const int slot = (1 + (d - 1) * k + j) * k + r;
+        const float cf = s_conf[slot];
+        const float v = conf_only ? cf : __fadd_rn(__fmul_rn(tkey_score(s_key[p]), cf), 0.0f);
+        s_key[nbase + q] = tree_key(v, p, s_tok[slot]);
+      }
     }
   }
   __syncthreads();
 
   // ---- selection in output order ----------------------------------------
-  if (full) {
-    const int *Lg = s_Lg + cur * m;
-    for (int q = tid; q < m; q += blockDim.x) s_sel[q] = Lg[q];
-  } else if (rerank && (tid >> 5) == 0) {
-    // confidence only: best-first growth by one warp, m picks of the
-    // greatest key whose parent is already in the tree (s_out >= 0)
-    const int lane = tid & 31;
+  const int *sel = full ? (s_Lg + cur * m) : s_sel;
+  if (!full && rerank) {
+    // confidence only: best-first growth, m picks of the greatest key whose
+    // parent is already in the tree (s_out >= 0); each pick is a block-wide
+    // arg-max (thread scan, warp shuffles, then the warps' winners)
+    __shared__ uint64_t s_wbest[kTreeThreads / 32];
+    __shared__ int s_wg[kTreeThreads / 32];
+    const int lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
     for (int pick = 0; pick < m; ++pick) {
       uint64_t best = 0;
       int bg = -1;
-      for (int g = 1 + lane; g <= NC; g += 32) {
+      for (int g = 1 + tid; g <= NC; g += blockDim.x) {
         const uint64_t key = s_key[g];
         if (s_out[g] < 0 && s_out[tkey_parent(key)] >= 0 && (bg < 0 || key > best)) {
           best = key;
@@ -233,55 +235,85 @@ __global__ void __launch_bounds__(kTreeThreads) tree_build_kernel(TreeArgs a) {
           bg = og;
         }
       }
-      if (bg < 0) {  // nothing left to add (cannot happen for m <= candidates)
-        if (lane == 0) s_bad = 1;
-        break;
-      }
       if (lane == 0) {
-        s_out[bg] = pick + 1;
-        s_sel[pick] = bg;
+        s_wbest[warp] = best;
+        s_wg[warp] = bg;
       }
-      __syncwarp();
+      __syncthreads();
+      if (warp == 0) {
+        best = lane < nwarps ? s_wbest[lane] : 0;
+        bg = lane < nwarps ? s_wg[lane] : -1;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const uint64_t ob = shfl_xor_u64(best, o);
+          const int og = __shfl_xor_sync(0xffffffffu, bg, o);
+          if (og >= 0 && (bg < 0 || ob > best)) {
+            best = ob;
+            bg = og;
+          }
+        }
+        if (lane == 0) {
+          if (bg < 0) {
+            s_bad = 1;  // nothing left to add (cannot happen for m <= candidates)
+            s_sel[pick] = 0;
+          } else {
+            s_out[bg] = pick + 1;
+            s_sel[pick] = bg;
+          }
+        }
+      }
+      __syncthreads();
     }
+  } else {
+    for (int q = tid; q < m; q += blockDim.x) s_out[sel[q]] = q + 1;
   }
   __syncthreads();
 
-  // ---- outputs ---------------------------------------------------------
-  for (int q = tid; q < m; q += blockDim.x) s_out[s_sel[q]] = q + 1;
-  __syncthreads();
+  // ---- outputs and mask ----------------------------------------------------
+  // thread (i, w): node i's fields (w == 0) and mask word w, the latter by
+  // walking node i's ancestors in candidate-id space (every ancestor of a
+  // selected candidate is selected; at most D+1 steps even on bad input)
   const int64_t ob = static_cast<int64_t>(b) * n;
-  for (int i = tid; i < n; i += blockDim.x) {
-    int t, par, dep, src, row;
-    float sc;
-    if (i == 0) {
-      t = a.root_tok ? a.root_tok[b] : -1;
-      par = -1; dep = 0; src = 0; row = 0; sc = 1.0f;
-    } else {
-      src = s_sel[i - 1];
-      const uint64_t key = s_key[src];
-      t = tkey_token(key);
-      sc = tkey_score(key);
-      par = s_out[tkey_parent(key)];
-      if (par < 0 || par >= i) s_bad = 1;  // not closed: a confidence outside [0, 1]
-      dep = depth_of_gid(src, k);
-      row = s_row[src];
+  const int W = (n + 63) >> 6;
+  for (int q = tid; q < n * W; q += blockDim.x) {
+    const int i = q / W, w = q % W;
+    const int src = i == 0 ? 0 : sel[i - 1];
+    if (w == 0) {
+      int t, par, dep, row;
+      float sc;
+      if (i == 0) {
+        t = a.root_tok ? a.root_tok[b] : -1;
+        par = -1; dep = 0; row = 0; sc = 1.0f;
+      } else {
+        const uint64_t key = s_key[src];
+        t = tkey_token(key);
+        sc = tkey_score(key);
+        par = s_out[tkey_parent(key)];
+        if (par < 0 || par >= i) s_bad = 1;  // not closed: a confidence outside [0, 1]
+        dep = depth_of_gid(src, k);
+        row = s_row[src];
+      }
+      a.node_tok[ob + i] = t;
+      a.node_parent[ob + i] = par;
+      if (a.node_depth) a.node_depth[ob + i] = dep;
+      if (a.node_score) a.node_score[ob + i] = sc;
+      if (a.node_src) a.node_src[ob + i] = src;
+      if (a.node_row) a.node_row[ob + i] = row;
     }
-    s_par[i] = par;
-    a.node_tok[ob + i] = t;
-    a.node_parent[ob + i] = par;
-    if (a.node_depth) a.node_depth[ob + i] = dep;
-    if (a.node_score) a.node_score[ob + i] = sc;
-    if (a.node_src) a.node_src[ob + i] = src;
-    if (a.node_row) a.node_row[ob + i] = row;
+    if (a.mask) {
+      uint64_t bits = 0;
+      int g = src;
+      for (int steps = 0; steps <= D; ++steps) {
+        const int node = s_out[g];
+        if (node >= 0 && (node >> 6) == w) bits |= 1ull << (node & 63);
+        if (g == 0) break;
+        g = tkey_parent(s_key[g]);
+        if (g < 0 || g > NC) break;
+      }
+      a.mask[(ob + i) * W + w] = bits;
+    }
   }
   __syncthreads();
-  if (a.mask) {
-    const int W = (n + 63) >> 6;
-    for (int q = tid; q < n * W; q += blockDim.x) {
-      const int i = q / W, w = q % W;
-      a.mask[(ob + i) * W + w] = mask_word(s_par, n, i, w);
-    }
-  }
   if (tid == 0 && s_bad) report(a.status, EAGLE_ERR_INVALID);
 }
 
@@ -303,14 +335,13 @@ __global__ void __launch_bounds__(256) tree_mask_kernel(const int32_t *parent, i
 
 size_t tree_smem_bytes(int D, int k, int m) {
   const int NC = k + (D - 1) * k * k;
-  const int kk = k * k, n = m + 1;
+  const int kk = k * k;
   size_t bytes = sizeof(uint64_t) * (NC + 1)          // s_key
                + sizeof(uint64_t) * 2 * m             // s_L
                + sizeof(int) * 2 * m                  // s_Lg
                + sizeof(int) * (2 * kk + m)           // s_cnt
                + sizeof(int) * 2 * (NC + 1)           // s_row, s_out
-               + sizeof(int) * n + sizeof(int) * k    // s_par, s_E
-               + sizeof(int) * m                      // s_sel
+               + sizeof(int) * m + sizeof(int) * k    // s_sel, s_E
                + 8 * static_cast<size_t>(1 + (D - 1) * k) * k;  // s_tok, s_conf
   return (bytes + 15) / 16 * 16;
 }
