@@ -193,3 +193,30 @@ def scaled(w: Workload, **changes):
     d = dict(w.__dict__)
     d.update(changes)
     return Workload(**d)
+
+
+# ---------------------------------------------------------------------------
+# static draft-tree templates (the EAGLE-1 style fixed tree is an input: the
+# pages say only that it is chosen offline and applied to every input)
+# ---------------------------------------------------------------------------
+
+# A synthetic 60-node template for D = 6, k = 10: per depth, the number of
+# children of that depth's nodes in node order (later nodes get none).
+STATIC_SHAPE_60 = ([10], [5, 4, 3, 2, 1], [4, 3, 3, 2, 2, 1, 1, 1], [3, 2, 2, 1, 1, 1, 1],
+                   [2, 1, 1, 1, 1], [1])
+
+
+def static_template(shape=STATIC_SHAPE_60):
+    """(parent, rank) int32 arrays of a template built from `shape`:
+    shape[d][j] children (ranks 0..c-1) for the j-th node of depth d."""
+    parent, rank = [-1], [0]
+    level = [0]
+    for counts in shape:
+        nxt = []
+        for j, c in enumerate(counts):
+            for r in range(c):
+                parent.append(level[j])
+                rank.append(r)
+                nxt.append(len(parent) - 1)
+        level = nxt
+    return np.array(parent, dtype=np.int32), np.array(rank, dtype=np.int32)
