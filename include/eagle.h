@@ -196,6 +196,34 @@ int eagle_tree_build_variant(const int32_t *tok, const float *conf, int B, int D
                              eagle_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Stage 2 for the EAGLE-1 static draft tree.
+ * [EAGLE-2] sections "背景" and "EAGLE-1からの変更点": EAGLE-1 places its draft
+ * tokens on a tree shape fixed in advance and applies it to every input;
+ * only the tokens come from the draft.  The shape is an input template:
+ *   tree_parent  device int32 [n]: -1 for node 0 (the root), else the parent
+ *                index, which must be smaller than the node's own
+ *   tree_rank    device int32 [n]: node i is the tree_rank[i]-th of its
+ *                parent's top-k draft tokens (0 <= rank < k, distinct among
+ *                siblings; entry 0 ignored)
+ * Draft rows: the root's distribution is row [0, 0]; the j-th node of depth
+ * d >= 1 that has children (in node order) uses row [d, j], so a depth may
+ * hold at most k such nodes and none at depth D.  Inputs tok/conf/root_tok
+ * and the outputs are those of eagle_tree_build with m = n - 1: node order is
+ * the template's, node_src = the template index, node_score = the float32
+ * product of the confidences on the root path, node_row = d*k + j for nodes
+ * with children (root 0), else -1; mask optional.
+ * Device errors: a template that breaks the rules above sets
+ * EAGLE_ERR_INVALID in *status (when given) and leaves the outputs unwritten.
+ * Limits: 1 <= k <= 32, 1 <= D <= 32, 1 <= n <= 1024.
+ * ------------------------------------------------------------------------ */
+int eagle_static_tree(const int32_t *tok, const float *conf, int B, int D, int k,
+                      const int32_t *tree_parent, const int32_t *tree_rank, int n,
+                      const int32_t *root_tok, int32_t *node_tok,
+                      int32_t *node_parent, int32_t *node_depth,
+                      float *node_score, int32_t *node_src, int32_t *node_row,
+                      uint64_t *mask, int32_t *status, eagle_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Ancestor-only attention mask.
  * [EAGLE-2] section "注意マスクの調整": each token attends only to its
  * ancestors.  Bit (j % 64) of word j / 64 of row i is set iff j == i or j is

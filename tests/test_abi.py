@@ -69,6 +69,13 @@ def test_invalid_arguments_are_rejected_on_the_host(lib):
     va[6] = 2                                   # D*k = 6 >= m = 5: accepted until launch, so use m = 7
     va[5] = 7
     assert lib.eagle_tree_build_variant(*va) == -1
+    # static_tree: template size and depth limits
+    sa = [fake, fake, 1, 3, 2, fake, fake, 0, NULL, fake, fake, NULL, NULL, NULL, NULL, NULL, NULL, NULL]
+    assert lib.eagle_static_tree(*sa) == -1
+    sa[7] = 1025
+    assert lib.eagle_static_tree(*sa) == -1
+    sa[7], sa[3] = 5, 33
+    assert lib.eagle_static_tree(*sa) == -1
     # tree_mask: n out of range
     assert lib.eagle_tree_mask(fake, 1, 0, fake, NULL) == -1
     assert lib.eagle_tree_mask(fake, 1, 5000, fake, NULL) == -1

@@ -9,6 +9,7 @@ library is missing or a call reports an error, an exception is raised.
     draft_topk  -> eagle_draft_topk   (softmax statistics + top-k per draft row)
     tree_build  -> eagle_tree_build   (global scores, expansion, rerank, mask;
                    eagle_tree_build_variant for the ablation flags)
+    static_tree -> eagle_static_tree  (EAGLE-1 static tree from a template)
     tree_mask   -> eagle_tree_mask    (ancestor-only attention mask)
     tree_attn   -> eagle_tree_attn    (tree-masked attention over the KV prefix)
     verify      -> eagle_verify       (greedy / speculative-sampling walk)
@@ -28,7 +29,7 @@ TREE_CONFIDENCE_ONLY, TREE_NO_RERANK = 1, 2
 EXPORTED = (
     "eagle_status_string", "eagle_version",
     "eagle_draft_topk_workspace_size", "eagle_draft_topk", "eagle_draft_topk_noalloc",
-    "eagle_tree_build", "eagle_tree_build_variant", "eagle_tree_mask",
+    "eagle_tree_build", "eagle_tree_build_variant", "eagle_static_tree", "eagle_tree_mask",
     "eagle_tree_attn_workspace_size", "eagle_tree_attn",
     "eagle_verify_workspace_size", "eagle_verify",
 )
@@ -57,6 +58,7 @@ def load_library(path=LIB_PATH):
         "eagle_draft_topk_noalloc": (I, [P, I, I, I, I, I, I64, P, P, P, P, P]),
         "eagle_tree_build": (I, [P, P, I, I, I, I, P, P, P, P, P, P, P, P, P, P]),
         "eagle_tree_build_variant": (I, [P, P, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P]),
+        "eagle_static_tree": (I, [P, P, I, I, I, P, P, I, P, P, P, P, P, P, P, P, P, P]),
         "eagle_tree_mask": (I, [P, I, I, P, P]),
         "eagle_tree_attn_workspace_size": (SZ, [I, I, I, I, I, I, I]),
         "eagle_tree_attn": (I, [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, P, P, P, SZ, P]),
@@ -191,6 +193,29 @@ def tree_build(tok, conf, m, root_tok=None, with_mask=True, out=None, status=Non
                                     _ptr(o["parent"]), _ptr(o["depth"]), _ptr(o["score"]),
                                     _ptr(o["src"]), _ptr(o["row"]), _ptr(o.get("mask")),
                                     _ptr(status), _stream(stream)), "eagle_tree_build")
+    return o
+
+
+def static_tree(tok, conf, tree_parent, tree_rank, root_tok=None, with_mask=True, out=None, status=None,
+                stream=None):
+    """EAGLE-1 static tree: tok/conf [B, D, k, k] and a template (tree_parent,
+    tree_rank int32 [n] on the device) -> node arrays [B, n] (+ mask)."""
+    lib = load_library()
+    _cuda(tok, "tok")
+    B, D, k, _ = tok.shape
+    n = int(tree_parent.shape[0])
+    dev = tok.device
+    W = (n + 63) // 64
+    o = out or {}
+    for key, dt in (("tok", torch.int32), ("parent", torch.int32), ("depth", torch.int32),
+                    ("score", torch.float32), ("src", torch.int32), ("row", torch.int32)):
+        o.setdefault(key, torch.empty((B, n), dtype=dt, device=dev))
+    if with_mask:
+        o.setdefault("mask", torch.empty((B, n, W), dtype=torch.int64, device=dev))
+    _check(lib.eagle_static_tree(_ptr(tok), _ptr(conf), B, D, k, _ptr(tree_parent), _ptr(tree_rank), n,
+                                 _ptr(root_tok), _ptr(o["tok"]), _ptr(o["parent"]), _ptr(o["depth"]),
+                                 _ptr(o["score"]), _ptr(o["src"]), _ptr(o["row"]), _ptr(o.get("mask")),
+                                 _ptr(status), _stream(stream)), "eagle_static_tree")
     return o
 
 

@@ -17,6 +17,11 @@ cudaError_t launch_tree_build(const int32_t *tok, const float *conf, int B, int 
                               int32_t *node_depth, float *node_score, int32_t *node_src,
                               int32_t *node_row, uint64_t *mask, int32_t *status, cudaStream_t st);
 cudaError_t launch_tree_mask(const int32_t *parent, int B, int n, uint64_t *mask, cudaStream_t st);
+// static_tree.cu
+cudaError_t launch_static_tree(const int32_t *tok, const float *conf, int B, int D, int k, const int32_t *parent,
+                               const int32_t *rank, int n, const int32_t *root_tok, int32_t *node_tok,
+                               int32_t *node_parent, int32_t *node_depth, float *node_score, int32_t *node_src,
+                               int32_t *node_row, uint64_t *mask, int32_t *status, cudaStream_t st);
 size_t tree_smem_bytes(int D, int k, int m);
 // tree_attn_simt.cu / tree_attn_tc.cu
 size_t attn_simt_workspace_bytes(int B, int n, int Hq, int dh, int Lmax, int num_sms);
@@ -122,6 +127,17 @@ int eagle_tree_build(const int32_t *tok, const float *conf, int B, int D, int k,
                      uint64_t *mask, int32_t *status, eagle_stream_t stream) {
   return eagle_tree_build_variant(tok, conf, B, D, k, m, 0, root_tok, node_tok, node_parent, node_depth,
                                   node_score, node_src, node_row, mask, status, stream);
+}
+
+int eagle_static_tree(const int32_t *tok, const float *conf, int B, int D, int k, const int32_t *tree_parent,
+                      const int32_t *tree_rank, int n, const int32_t *root_tok, int32_t *node_tok,
+                      int32_t *node_parent, int32_t *node_depth, float *node_score, int32_t *node_src,
+                      int32_t *node_row, uint64_t *mask, int32_t *status, eagle_stream_t stream) {
+  if (!tok || !conf || !tree_parent || !tree_rank || !node_tok || !node_parent) return EAGLE_ERR_INVALID;
+  if (B < 1 || D < 1 || D > 32 || k < 1 || k > 32 || n < 1 || n > 1024) return EAGLE_ERR_INVALID;
+  return from_cuda(launch_static_tree(tok, conf, B, D, k, tree_parent, tree_rank, n, root_tok, node_tok,
+                                      node_parent, node_depth, node_score, node_src, node_row, mask, status,
+                                      reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int eagle_tree_mask(const int32_t *node_parent, int B, int n, uint64_t *mask, eagle_stream_t stream) {
