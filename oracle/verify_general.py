@@ -25,8 +25,11 @@ Readings for the tree (the page describes a chain):
     they agree).  Child i is accepted iff u * S_{i-1} * q(t) < R_{i-1}(t).
   * If a residual sums to exactly 0 (p <= C q everywhere), the draw falls
     back to p.  Temperature T scales both logit rows.
-Decisions within a relative 1e-5 of their boundary are flagged (`ambiguous`)
-so float32 implementations can be compared up to that point.
+Decisions within 1e-5 of their boundary are flagged (`ambiguous`) so float32
+implementations can be compared up to that point.  The band is measured
+against the terms that cancel in R = max(0, p - C q): 1e-5 * (p(t) +
+(C + S) q(t)) for an acceptance, 1e-5 * (1 + C) (probability units) for the
+bonus draw, since a float32 residual cannot resolve finer than that.
 """
 from dataclasses import dataclass
 
@@ -49,14 +52,15 @@ class Walk:
     ambiguous: tuple = None
 
 
-def draw_inverse_cdf(R, S, u):
-    """Smallest v with cumsum(R)[v] > u * S; ambiguity margin relative to S."""
+def draw_inverse_cdf(R, S, u, band):
+    """Smallest v with cumsum(R)[v] > u * S; flagged when the threshold is
+    within `band` of the chosen token's cumulative bounds."""
     c = np.cumsum(R)
     thr = u * S
     v = int(np.searchsorted(c, thr, side="right"))
     v = min(v, len(R) - 1)
     lo = c[v - 1] if v > 0 else 0.0
-    amb = abs(thr - lo) <= AMBIG * S or abs(c[v] - thr) <= AMBIG * S
+    amb = abs(thr - lo) <= band or abs(c[v] - thr) <= band
     return v, amb
 
 
@@ -71,28 +75,29 @@ def verify_tree(target, q_logits_of, node_tok, node_parent, T, u):
     cur, path, tokens, amb = 0, [0], [], None
     while True:
         p = softmax_T(target[cur], T)
-        R, S = p, 1.0
+        R, S, C = p, 1.0, 0.0       # C: the closed form's multiple of q (band only)
         accepted = None
         if kids[cur]:
             q = softmax_T(q_logits_of(cur), T)
             for x in kids[cur]:
                 t = int(node_tok[x])
                 lhs, rhs = u[x, 0] * S * q[t], R[t]
-                if amb is None and abs(lhs - rhs) <= AMBIG * max(S * q[t], 1e-300):
+                if amb is None and abs(lhs - rhs) <= AMBIG * max(p[t] + (C + S) * q[t], 1e-300):
                     amb = (len(path) - 1, "accept", x)
                 if lhs < rhs:
                     accepted = x
                     break
                 R = np.maximum(0.0, R - S * q)
+                C += S
                 S = float(R.sum())
                 if S == 0.0:
-                    R, S = p, 1.0
+                    R, S, C = p, 1.0, 0.0
         if accepted is not None:
             cur = accepted
             path.append(cur)
             tokens.append(int(node_tok[cur]))
             continue
-        v, a = draw_inverse_cdf(R, S, u[cur, 1])
+        v, a = draw_inverse_cdf(R, S, u[cur, 1], AMBIG * (1.0 + C))
         if amb is None and a:
             amb = (len(path) - 1, "bonus", cur)
         tokens.append(v)
