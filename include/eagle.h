@@ -307,6 +307,44 @@ int eagle_verify(const void *target, int dtype, int64_t ld,
                  void *workspace, size_t workspace_bytes,
                  eagle_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Stage 4 with draft distributions — speculative-sampling verification of a
+ * tree whose tokens were drawn from the draft's distribution q.
+ * [EAGLE-1] section "検証方法": a drafted token t is accepted with
+ * probability min(1, p(t)/q(t)); after a rejection the target distribution is
+ * replaced by the residual norm(max(0, p - q)) and a token is finally drawn
+ * from it, so the output follows the target exactly.  Tree form: at node cur
+ * the children (node-index order, all drafted from q = softmax(draft row of
+ * cur / T)) are tested in turn against the current residual R = max(0, p -
+ * C q) with normaliser S (C = 0, S = 1 before any rejection; a rejection
+ * adds S to C and S becomes sum over the vocabulary of the new R):
+ *   child x with token t is accepted iff u[b,x,0] * S * q(t) < R(t);
+ * with no child accepted (or at a leaf) the bonus is the smallest token
+ * whose cumulative R exceeds u[b,cur,1] * sum(R).  A residual that sums to 0
+ * is replaced by p.  p = softmax(target row / T).
+ *   target     dtype, row (b, i) at element (b*(m+1) + i) * ld_t
+ *   draft      dtype, draft logits [B, D, k, V], row (b, d, j) at element
+ *              ((b*D + d)*k + j) * ld_d (the rows eagle_draft_topk reads)
+ *   node_tok, node_parent, node_row   device int32 [B, m+1] as stage 2
+ *              writes them; node_row[b, i] = d*k + j names the draft row of
+ *              every node that has children
+ *   uniforms   device float [B, m+1, 2] in [0, 1)
+ *   accept_len, path_nodes, out_tokens, status   as in eagle_verify
+ * No workspace: one CTA per sequence keeps its state in shared memory.
+ * Device errors: a node with children whose node_row is outside [0, D*k),
+ * a token outside [0, V) or no residual mass set EAGLE_ERR_INVALID.
+ * Limits: temperature > 0; V*elemsize, ld_t*elemsize and ld_d*elemsize
+ * multiples of 16 bytes; 16-byte aligned logits; 1 <= m+1 <= 4096;
+ * 1 <= D; 1 <= k <= 32.
+ * ------------------------------------------------------------------------ */
+int eagle_verify_draft(const void *target, const void *draft, int dtype,
+                       int64_t ld_t, int64_t ld_d, const int32_t *node_tok,
+                       const int32_t *node_parent, const int32_t *node_row,
+                       int B, int m, int D, int k, int V, float temperature,
+                       const float *uniforms, int32_t *accept_len,
+                       int32_t *path_nodes, int32_t *out_tokens,
+                       int32_t *status, eagle_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -13,6 +13,7 @@ library is missing or a call reports an error, an exception is raised.
     tree_mask   -> eagle_tree_mask    (ancestor-only attention mask)
     tree_attn   -> eagle_tree_attn    (tree-masked attention over the KV prefix)
     verify      -> eagle_verify       (greedy / speculative-sampling walk)
+    verify_draft -> eagle_verify_draft (sampling walk against draft distributions q)
 """
 import ctypes
 import os
@@ -31,7 +32,7 @@ EXPORTED = (
     "eagle_draft_topk_workspace_size", "eagle_draft_topk", "eagle_draft_topk_noalloc",
     "eagle_tree_build", "eagle_tree_build_variant", "eagle_static_tree", "eagle_tree_mask",
     "eagle_tree_attn_workspace_size", "eagle_tree_attn",
-    "eagle_verify_workspace_size", "eagle_verify",
+    "eagle_verify_workspace_size", "eagle_verify", "eagle_verify_draft",
 )
 
 _lib = None
@@ -64,6 +65,7 @@ def load_library(path=LIB_PATH):
         "eagle_tree_attn": (I, [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, P, P, P, SZ, P]),
         "eagle_verify_workspace_size": (SZ, [I, I, I]),
         "eagle_verify": (I, [P, I, I64, P, P, I, I, I, I, I, F, P, P, P, P, P, P, SZ, P]),
+        "eagle_verify_draft": (I, [P, P, I, I64, I64, P, P, P, I, I, I, I, I, F, P, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -276,4 +278,26 @@ def verify(target, node_tok, node_parent, D, mode, temperature=1.0, uniforms=Non
                             B, m, D, V, mode_code, ctypes.c_float(temperature), _ptr(uniforms),
                             _ptr(accept_len), _ptr(path_nodes), _ptr(out_tokens), _ptr(status),
                             _ptr(wbuf), wbytes, _stream(stream)), "eagle_verify")
+    return accept_len, path_nodes, out_tokens
+
+
+def verify_draft(target, draft, node_tok, node_parent, node_row, D, temperature, uniforms, accept_len=None,
+                 path_nodes=None, out_tokens=None, status=None, stream=None):
+    """Speculative-sampling verification against the draft distributions:
+    target [B, m+1, V] and draft [B, D, k, V] logits (same dtype), node
+    arrays [B, m+1] -> (accept_len [B], path_nodes [B, D+1], out_tokens [B, D+1])."""
+    lib = load_library()
+    _cuda(target, "target")
+    B, n, V = target.shape
+    k = draft.shape[2]
+    assert draft.shape[0] == B and draft.shape[1] == D and draft.dtype == target.dtype
+    dev = target.device
+    accept_len = accept_len if accept_len is not None else torch.empty(B, dtype=torch.int32, device=dev)
+    path_nodes = path_nodes if path_nodes is not None else torch.empty((B, D + 1), dtype=torch.int32, device=dev)
+    out_tokens = out_tokens if out_tokens is not None else torch.empty((B, D + 1), dtype=torch.int32, device=dev)
+    _check(lib.eagle_verify_draft(_ptr(target), _ptr(draft), _dtype_code(target), target.stride(1),
+                                  draft.stride(2), _ptr(node_tok), _ptr(node_parent), _ptr(node_row), B, n - 1,
+                                  D, k, V, ctypes.c_float(temperature), _ptr(uniforms), _ptr(accept_len),
+                                  _ptr(path_nodes), _ptr(out_tokens), _ptr(status), _stream(stream)),
+           "eagle_verify_draft")
     return accept_len, path_nodes, out_tokens

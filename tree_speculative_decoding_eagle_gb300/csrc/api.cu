@@ -17,6 +17,12 @@ cudaError_t launch_tree_build(const int32_t *tok, const float *conf, int B, int 
                               int32_t *node_depth, float *node_score, int32_t *node_src,
                               int32_t *node_row, uint64_t *mask, int32_t *status, cudaStream_t st);
 cudaError_t launch_tree_mask(const int32_t *parent, int B, int n, uint64_t *mask, cudaStream_t st);
+// verify_draft.cu
+cudaError_t launch_verify_draft(const void *target, const void *draft, int dtype, int64_t ld_t, int64_t ld_d,
+                                const int32_t *node_tok, const int32_t *node_parent, const int32_t *node_row,
+                                int B, int m, int D, int k, int V, float temperature, const float *uniforms,
+                                int32_t *accept_len, int32_t *path_nodes, int32_t *out_tokens, int32_t *status,
+                                cudaStream_t st);
 // static_tree.cu
 cudaError_t launch_static_tree(const int32_t *tok, const float *conf, int B, int D, int k, const int32_t *parent,
                                const int32_t *rank, int n, const int32_t *root_tok, int32_t *node_tok,
@@ -200,6 +206,26 @@ int eagle_verify(const void *target, int dtype, int64_t ld, const int32_t *node_
   return from_cuda(launch_verify(target, dtype, ld, node_tok, node_parent, B, m, D, V, mode,
                                  temperature, uniforms, accept_len, path_nodes, out_tokens, status,
                                  workspace, current_num_sms(), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int eagle_verify_draft(const void *target, const void *draft, int dtype, int64_t ld_t, int64_t ld_d,
+                       const int32_t *node_tok, const int32_t *node_parent, const int32_t *node_row, int B,
+                       int m, int D, int k, int V, float temperature, const float *uniforms,
+                       int32_t *accept_len, int32_t *path_nodes, int32_t *out_tokens, int32_t *status,
+                       eagle_stream_t stream) {
+  if (!target || !draft || !node_tok || !node_parent || !node_row || !uniforms || !accept_len || !path_nodes ||
+      !out_tokens)
+    return EAGLE_ERR_INVALID;
+  if (!valid_dtype(dtype) || B < 1 || m < 0 || m + 1 > 4096 || D < 1 || k < 1 || k > 32 || V < 1)
+    return EAGLE_ERR_INVALID;
+  if (ld_t < V || ld_d < V || !(temperature > 0.f)) return EAGLE_ERR_INVALID;
+  const int es = elem_size(dtype);
+  if ((static_cast<int64_t>(V) * es) % 16 || (ld_t * es) % 16 || (ld_d * es) % 16 || !aligned16(target) ||
+      !aligned16(draft))
+    return EAGLE_ERR_INVALID;
+  return from_cuda(launch_verify_draft(target, draft, dtype, ld_t, ld_d, node_tok, node_parent, node_row, B, m,
+                                       D, k, V, temperature, uniforms, accept_len, path_nodes, out_tokens, status,
+                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"
