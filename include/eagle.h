@@ -272,6 +272,36 @@ int eagle_tree_attn(const void *q, const void *k_cache, const void *v_cache,
                     size_t workspace_bytes, eagle_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Stage 3 over a paged KV prefix (block-table attention).
+ * Same computation as eagle_tree_attn; the prefix K/V live in page pools
+ *   k_pages, v_pages  bf16 [num_pages, Hkv, page_size, dh]
+ *   block_table       device int32 [B, max_pages]: logical page p of
+ *                     sequence b is physical page block_table[b, p]
+ * so prefix position L of sequence b is row L % page_size of page
+ * block_table[b, L / page_size] (entries for pages at or beyond kv_len are
+ * not read).  kv_len[b] is clamped to max_pages * page_size.  Other
+ * arguments as in eagle_tree_attn.  Workspace from
+ * eagle_tree_attn_paged_workspace_size.
+ * Device errors: a block-table entry outside [0, num_pages) for a page the
+ * prefix uses sets EAGLE_ERR_INVALID (page 0 is read in its place).
+ * Limits: bf16 only (other dtypes EAGLE_ERR_UNSUPPORTED); dh in {64, 128};
+ * page_size a power of two in [16, 4096]; max_pages * page_size <= 2^24.
+ * ------------------------------------------------------------------------ */
+size_t eagle_tree_attn_paged_workspace_size(int dtype, int B, int n, int Hq,
+                                            int Hkv, int dh, int max_pages,
+                                            int page_size);
+
+int eagle_tree_attn_paged(const void *q, const void *k_pages,
+                          const void *v_pages, const int32_t *block_table,
+                          int max_pages, int page_size, int num_pages,
+                          const int32_t *kv_len, const void *k_tree,
+                          const void *v_tree, const uint64_t *mask, int dtype,
+                          int B, int n, int Hq, int Hkv, int dh, float scale,
+                          void *out, float *lse, int32_t *status,
+                          void *workspace, size_t workspace_bytes,
+                          eagle_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Stage 4 — verification walk.
  * [EAGLE-1] section "検証方法": each draft token is accepted or rejected by
  * the ratio of target and draft distributions; after a rejection the rest is
@@ -344,6 +374,35 @@ int eagle_verify_draft(const void *target, const void *draft, int dtype,
                        const float *uniforms, int32_t *accept_len,
                        int32_t *path_nodes, int32_t *out_tokens,
                        int32_t *status, eagle_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * After verification — commit the accepted path's keys and values.
+ * [EAGLE-1] section "検証方法" / [EAGLE-2]: the accepted draft tokens become
+ * part of the sequence; everything after a rejection is discarded.  The
+ * root's K/V is already the last prefix position.  For each sequence b with
+ * a = accept_len[b], nodes path_nodes[b, 1..a] (as eagle_verify writes them)
+ * have their rows of k_tree/v_tree [B, Hkv, n, dh] copied, in path order, to
+ * positions kv_len[b] .. kv_len[b]+a-1 of the cache, and kv_len[b] becomes
+ * kv_len[b] + a (updated in place).
+ *   cache        block_table == NULL: contiguous k_cache/v_cache
+ *                [B, Hkv, Lmax, dh]; otherwise page pools [num_pages, Hkv,
+ *                page_size, dh] addressed through block_table [B, max_pages]
+ *                (the caller has mapped the pages the new positions need)
+ *   slot_mapping device int32 [B, n] (out, may be NULL): node i's position
+ *                after the commit (root kv_len-1), -1 for nodes not kept
+ * Device errors: a path node outside [1, n), a = accept_len outside [0, D],
+ * kv_len < 1, or new positions beyond the cache (Lmax, or an unmapped page)
+ * set EAGLE_ERR_INVALID and leave that sequence unchanged.
+ * Limits: dh*elemsize a multiple of 16 bytes; 1 <= D <= 64; n <= 4096; page
+ * rules as for eagle_tree_attn_paged.
+ * ------------------------------------------------------------------------ */
+int eagle_kv_commit(const void *k_tree, const void *v_tree, int dtype, int B,
+                    int n, int Hkv, int dh, const int32_t *accept_len,
+                    const int32_t *path_nodes, int D, void *k_cache,
+                    void *v_cache, int Lmax, const int32_t *block_table,
+                    int max_pages, int page_size, int num_pages,
+                    int32_t *kv_len, int32_t *slot_mapping, int32_t *status,
+                    eagle_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -12,6 +12,8 @@ library is missing or a call reports an error, an exception is raised.
     static_tree -> eagle_static_tree  (EAGLE-1 static tree from a template)
     tree_mask   -> eagle_tree_mask    (ancestor-only attention mask)
     tree_attn   -> eagle_tree_attn    (tree-masked attention over the KV prefix)
+    tree_attn_paged -> eagle_tree_attn_paged (the same over a paged prefix)
+    kv_commit   -> eagle_kv_commit    (accepted path's K/V into the cache)
     verify      -> eagle_verify       (greedy / speculative-sampling walk)
     verify_draft -> eagle_verify_draft (sampling walk against draft distributions q)
 """
@@ -32,6 +34,7 @@ EXPORTED = (
     "eagle_draft_topk_workspace_size", "eagle_draft_topk", "eagle_draft_topk_noalloc",
     "eagle_tree_build", "eagle_tree_build_variant", "eagle_static_tree", "eagle_tree_mask",
     "eagle_tree_attn_workspace_size", "eagle_tree_attn",
+    "eagle_tree_attn_paged_workspace_size", "eagle_tree_attn_paged", "eagle_kv_commit",
     "eagle_verify_workspace_size", "eagle_verify", "eagle_verify_draft",
 )
 
@@ -63,6 +66,9 @@ def load_library(path=LIB_PATH):
         "eagle_tree_mask": (I, [P, I, I, P, P]),
         "eagle_tree_attn_workspace_size": (SZ, [I, I, I, I, I, I, I]),
         "eagle_tree_attn": (I, [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, P, P, P, SZ, P]),
+        "eagle_tree_attn_paged_workspace_size": (SZ, [I, I, I, I, I, I, I, I]),
+        "eagle_tree_attn_paged": (I, [P, P, P, P, I, I, I, P, P, P, P, I, I, I, I, I, I, F, P, P, P, P, SZ, P]),
+        "eagle_kv_commit": (I, [P, P, I, I, I, I, I, P, P, I, P, P, I, P, I, I, I, P, P, P, P]),
         "eagle_verify_workspace_size": (SZ, [I, I, I]),
         "eagle_verify": (I, [P, I, I64, P, P, I, I, I, I, I, F, P, P, P, P, P, P, SZ, P]),
         "eagle_verify_draft": (I, [P, P, I, I64, I64, P, P, P, I, I, I, I, I, F, P, P, P, P, P, P]),
@@ -301,3 +307,49 @@ def verify_draft(target, draft, node_tok, node_parent, node_row, D, temperature,
                                   _ptr(path_nodes), _ptr(out_tokens), _ptr(status), _stream(stream)),
            "eagle_verify_draft")
     return accept_len, path_nodes, out_tokens
+
+
+def tree_attn_paged(q, k_pages, v_pages, block_table, kv_len, k_tree, v_tree, mask, scale=None, out=None,
+                    lse=None, workspace=None, status=None, stream=None):
+    """Tree attention over a paged prefix: k_pages/v_pages [num_pages, Hkv,
+    page_size, dh], block_table int32 [B, max_pages]; else as tree_attn."""
+    lib = load_library()
+    _cuda(q, "q")
+    B, n, Hq, dh = q.shape
+    num_pages, Hkv, page_size, _ = k_pages.shape
+    max_pages = block_table.shape[1]
+    scale = dh ** -0.5 if scale is None else scale
+    out = out if out is not None else torch.empty_like(q)
+    lse = lse if lse is not None else torch.empty((B, n, Hq), dtype=torch.float32, device=q.device)
+    ws = workspace or Workspace(q.device)
+    dt = _dtype_code(q)
+    wbuf, wbytes = ws.get(lib.eagle_tree_attn_paged_workspace_size(dt, B, n, Hq, Hkv, dh, max_pages, page_size))
+    _check(lib.eagle_tree_attn_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), max_pages,
+                                     page_size, num_pages, _ptr(kv_len), _ptr(k_tree), _ptr(v_tree), _ptr(mask),
+                                     dt, B, n, Hq, Hkv, dh, ctypes.c_float(scale), _ptr(out), _ptr(lse),
+                                     _ptr(status), _ptr(wbuf), wbytes, _stream(stream)), "eagle_tree_attn_paged")
+    return out, lse
+
+
+def kv_commit(k_tree, v_tree, accept_len, path_nodes, k_cache, v_cache, kv_len, block_table=None,
+              slot_mapping=None, status=None, stream=None):
+    """Append the accepted path's K/V rows to the cache (contiguous [B, Hkv,
+    Lmax, dh], or page pools [num_pages, Hkv, page_size, dh] with a
+    block_table); kv_len is updated in place.  Returns slot_mapping [B, n]."""
+    lib = load_library()
+    _cuda(k_tree, "k_tree")
+    B, Hkv, n, dh = k_tree.shape
+    D = path_nodes.shape[1] - 1
+    if slot_mapping is None:
+        slot_mapping = torch.empty((B, n), dtype=torch.int32, device=k_tree.device)
+    if block_table is None:
+        Lmax, max_pages, page_size, num_pages = k_cache.shape[2], 0, 0, 0
+    else:
+        Lmax = 0
+        num_pages, _, page_size, _ = k_cache.shape
+        max_pages = block_table.shape[1]
+    _check(lib.eagle_kv_commit(_ptr(k_tree), _ptr(v_tree), _dtype_code(k_tree), B, n, Hkv, dh, _ptr(accept_len),
+                               _ptr(path_nodes), D, _ptr(k_cache), _ptr(v_cache), Lmax, _ptr(block_table),
+                               max_pages, page_size, num_pages, _ptr(kv_len), _ptr(slot_mapping), _ptr(status),
+                               _stream(stream)), "eagle_kv_commit")
+    return slot_mapping

@@ -23,6 +23,19 @@ cudaError_t launch_verify_draft(const void *target, const void *draft, int dtype
                                 int B, int m, int D, int k, int V, float temperature, const float *uniforms,
                                 int32_t *accept_len, int32_t *path_nodes, int32_t *out_tokens, int32_t *status,
                                 cudaStream_t st);
+// tree_attn_tc.cu (paged prefix)
+cudaError_t launch_tree_attn_tc_paged(const void *q, const void *k_pages, const void *v_pages,
+                                      const int32_t *block_table, int max_pages, int page_size, int num_pages,
+                                      const int32_t *kv_len, const void *k_tree, const void *v_tree,
+                                      const uint64_t *mask, int B, int n, int Hq, int Hkv, int dh, float scale,
+                                      void *out, float *lse, void *ws, int32_t *status, int num_sms,
+                                      cudaStream_t st);
+// kv_commit.cu
+cudaError_t launch_kv_commit(const void *k_tree, const void *v_tree, int dtype, int B, int n, int Hkv, int dh,
+                             const int32_t *accept_len, const int32_t *path_nodes, int D, void *k_cache,
+                             void *v_cache, int Lmax, const int32_t *block_table, int max_pages, int page_size,
+                             int num_pages, int32_t *kv_len, int32_t *slot_mapping, int32_t *status,
+                             cudaStream_t st);
 // static_tree.cu
 cudaError_t launch_static_tree(const int32_t *tok, const float *conf, int B, int D, int k, const int32_t *parent,
                                const int32_t *rank, int n, const int32_t *root_tok, int32_t *node_tok,
@@ -181,6 +194,57 @@ int eagle_tree_attn(const void *q, const void *k_cache, const void *v_cache, con
   if (workspace_bytes < need || (need && !workspace)) return EAGLE_ERR_WORKSPACE;
   return from_cuda(launch_tree_attn_simt(q, k_cache, v_cache, kv_len, k_tree, v_tree, mask, dtype, B, n, Hq,
                                          Hkv, dh, Lmax, scale, out, lse, workspace, sms, st));
+}
+
+static bool valid_pages(int max_pages, int page_size, int num_pages) {
+  return max_pages >= 1 && num_pages >= 1 && page_size >= 16 && page_size <= 4096 &&
+         (page_size & (page_size - 1)) == 0 && static_cast<int64_t>(max_pages) * page_size <= (1 << 24);
+}
+
+size_t eagle_tree_attn_paged_workspace_size(int dtype, int B, int n, int Hq, int Hkv, int dh, int max_pages,
+                                            int page_size) {
+  if (dtype != EAGLE_BF16 || B < 1 || n < 1 || Hq < 1 || Hkv < 1 || dh < 1 || max_pages < 1 || page_size < 1)
+    return 0;
+  return attn_tc_workspace_bytes(B, n, Hq, Hkv, dh, max_pages * page_size, current_num_sms());
+}
+
+int eagle_tree_attn_paged(const void *q, const void *k_pages, const void *v_pages, const int32_t *block_table,
+                          int max_pages, int page_size, int num_pages, const int32_t *kv_len, const void *k_tree,
+                          const void *v_tree, const uint64_t *mask, int dtype, int B, int n, int Hq, int Hkv,
+                          int dh, float scale, void *out, float *lse, int32_t *status, void *workspace,
+                          size_t workspace_bytes, eagle_stream_t stream) {
+  if (!q || !k_pages || !v_pages || !block_table || !kv_len || !k_tree || !v_tree || !mask || !out)
+    return EAGLE_ERR_INVALID;
+  if (!valid_dtype(dtype) || B < 1 || n < 1 || n > 4096 || Hq < 1 || Hkv < 1 || Hq % Hkv ||
+      !valid_pages(max_pages, page_size, num_pages))
+    return EAGLE_ERR_INVALID;
+  if (dtype != EAGLE_BF16 || (dh != 64 && dh != 128)) return EAGLE_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(B) * Hkv > 65535) return EAGLE_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(k_tree) || !aligned16(v_tree) ||
+      !aligned16(out))
+    return EAGLE_ERR_INVALID;
+  const int sms = current_num_sms();
+  const size_t need = attn_tc_workspace_bytes(B, n, Hq, Hkv, dh, max_pages * page_size, sms);
+  if (workspace_bytes < need || (need && !workspace)) return EAGLE_ERR_WORKSPACE;
+  return from_cuda(launch_tree_attn_tc_paged(q, k_pages, v_pages, block_table, max_pages, page_size, num_pages,
+                                             kv_len, k_tree, v_tree, mask, B, n, Hq, Hkv, dh, scale, out, lse,
+                                             workspace, status, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int eagle_kv_commit(const void *k_tree, const void *v_tree, int dtype, int B, int n, int Hkv, int dh,
+                    const int32_t *accept_len, const int32_t *path_nodes, int D, void *k_cache, void *v_cache,
+                    int Lmax, const int32_t *block_table, int max_pages, int page_size, int num_pages,
+                    int32_t *kv_len, int32_t *slot_mapping, int32_t *status, eagle_stream_t stream) {
+  if (!k_tree || !v_tree || !accept_len || !path_nodes || !k_cache || !v_cache || !kv_len) return EAGLE_ERR_INVALID;
+  if (!valid_dtype(dtype) || B < 1 || n < 1 || n > 4096 || Hkv < 1 || dh < 1 || D < 1 || D > 64)
+    return EAGLE_ERR_INVALID;
+  if ((dh * elem_size(dtype)) % 16) return EAGLE_ERR_INVALID;
+  if (block_table ? !valid_pages(max_pages, page_size, num_pages) : Lmax < 1) return EAGLE_ERR_INVALID;
+  if (!aligned16(k_tree) || !aligned16(v_tree) || !aligned16(k_cache) || !aligned16(v_cache))
+    return EAGLE_ERR_INVALID;
+  return from_cuda(launch_kv_commit(k_tree, v_tree, dtype, B, n, Hkv, dh, accept_len, path_nodes, D, k_cache,
+                                    v_cache, Lmax, block_table, max_pages, page_size, num_pages, kv_len,
+                                    slot_mapping, status, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t eagle_verify_workspace_size(int B, int m, int V) {

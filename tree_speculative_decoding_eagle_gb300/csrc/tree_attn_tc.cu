@@ -43,6 +43,12 @@ struct TcArgs {
   const int32_t *kv_len;
   const uint64_t *mask;
   int B, n, Hq, Hkv, G, Lmax, S, W;
+  // paged prefix (block_table != nullptr): k_cache / v_cache are page pools
+  // [num_pages, Hkv, page_size, dh]; logical position L of sequence b is row
+  // L % page_size of page block_table[b * max_pages + L / page_size].  TMA
+  // boxes are page_box = min(page_size, NK) rows.
+  const int32_t *block_table;
+  int max_pages, page_size, page_box, num_pages;
   float scale_log2;  // softmax scale times log2(e)
   __nv_bfloat16 *out;
   float *lse;
@@ -168,26 +174,55 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
       if (!prefix || valid == NK) {
         if (lane == 0) {
           mbar_arrive_expect_tx(&kv_full[st], Sh::kStageBytes);
-          const CUtensorMap *km = prefix ? &kc_map : &kt_map;
-          const CUtensorMap *vm = prefix ? &vc_map : &vt_map;
-          const int row0 = prefix ? bg * a.Lmax + key0 : bg * n + key0;
+          if (prefix && a.block_table) {
+            // one box per page-sized piece of the tile, each at its page's row
+            for (int s0 = 0; s0 < NK; s0 += a.page_box) {
+              const int key = key0 + s0;
+              int page = a.block_table[static_cast<int64_t>(b) * a.max_pages + key / a.page_size];
+              if (page < 0 || page >= a.num_pages) {  // outside the pool: report, read page 0
+                report(a.status, EAGLE_ERR_INVALID);
+                page = 0;
+              }
+              const int row = (page * a.Hkv + g) * a.page_size + key % a.page_size;
 #pragma unroll
-          for (int r = 0; r < Sh::kRegions; ++r) {
-            tma_load_2d(kst + r * NK * 128, km, r * 64, row0, &kv_full[st]);
-            tma_load_2d(vst + r * NK * 128, vm, r * 64, row0, &kv_full[st]);
+              for (int r = 0; r < Sh::kRegions; ++r) {
+                tma_load_2d(kst + r * NK * 128 + s0 * 128, &kc_map, r * 64, row, &kv_full[st]);
+                tma_load_2d(vst + r * NK * 128 + s0 * 128, &vc_map, r * 64, row, &kv_full[st]);
+              }
+            }
+          } else {
+            const CUtensorMap *km = prefix ? &kc_map : &kt_map;
+            const CUtensorMap *vm = prefix ? &vc_map : &vt_map;
+            const int row0 = prefix ? bg * a.Lmax + key0 : bg * n + key0;
+#pragma unroll
+            for (int r = 0; r < Sh::kRegions; ++r) {
+              tma_load_2d(kst + r * NK * 128, km, r * 64, row0, &kv_full[st]);
+              tma_load_2d(vst + r * NK * 128, vm, r * 64, row0, &kv_full[st]);
+            }
           }
         }
       } else {
         // ragged last prefix tile: rows >= valid are zero (cache memory past
         // kv_len is never read)
-        const __nv_bfloat16 *kg = a.k_cache + (static_cast<int64_t>(bg) * a.Lmax + key0) * DH;
-        const __nv_bfloat16 *vg = a.v_cache + (static_cast<int64_t>(bg) * a.Lmax + key0) * DH;
         for (int idx = lane; idx < NK * (DH / 8); idx += 32) {
           const int r = idx / (DH / 8), c = idx % (DH / 8);
           uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
           if (r < valid) {
-            kv = *reinterpret_cast<const uint4 *>(kg + r * DH + c * 8);
-            vv = *reinterpret_cast<const uint4 *>(vg + r * DH + c * 8);
+            int64_t row;
+            if (a.block_table) {
+              const int key = key0 + r;
+              const int page = a.block_table[static_cast<int64_t>(b) * a.max_pages + key / a.page_size];
+              row = (page >= 0 && page < a.num_pages)
+                        ? (static_cast<int64_t>(page) * a.Hkv + g) * a.page_size + key % a.page_size
+                        : -1;
+              if (row < 0) report(a.status, EAGLE_ERR_INVALID);
+            } else {
+              row = static_cast<int64_t>(bg) * a.Lmax + key0 + r;
+            }
+            if (row >= 0) {
+              kv = *reinterpret_cast<const uint4 *>(a.k_cache + row * DH + c * 8);
+              vv = *reinterpret_cast<const uint4 *>(a.v_cache + row * DH + c * 8);
+            }
           }
           const uint32_t off = (c / 8) * (NK * 128) + sw128_offset(r, c % 8);
           *reinterpret_cast<uint4 *>(kst + off) = kv;
@@ -548,16 +583,21 @@ static cudaError_t launch_tc_t(const CUtensorMap *maps, const TcArgs &a, const T
   return cudaGetLastError();
 }
 
-cudaError_t launch_tree_attn_tc(const void *q, const void *k_cache, const void *v_cache, const int32_t *kv_len,
-                                const void *k_tree, const void *v_tree, const uint64_t *mask, int B, int n,
-                                int Hq, int Hkv, int dh, int Lmax, float scale, void *out, float *lse, void *ws,
-                                int32_t *status, int num_sms, cudaStream_t st) {
+// Common launcher; block_table == nullptr is the contiguous cache, otherwise
+// the page pools with Lmax = max_pages * page_size logical positions.
+static cudaError_t launch_tc_common(const void *q, const void *k_cache, const void *v_cache, const int32_t *kv_len,
+                                    const void *k_tree, const void *v_tree, const uint64_t *mask, int B, int n,
+                                    int Hq, int Hkv, int dh, int Lmax, float scale, void *out, float *lse,
+                                    void *ws, int32_t *status, int num_sms, cudaStream_t st,
+                                    const int32_t *block_table, int max_pages, int page_size, int num_pages) {
   const TcPlan p = tc_plan(B, n, Hq, Hkv, dh, Lmax, num_sms);
   CUtensorMap maps[4];
-  const int64_t cache_rows = static_cast<int64_t>(B) * Hkv * Lmax;
+  const int page_box = block_table ? min(page_size, p.NK) : p.NK;
+  const int64_t cache_rows = block_table ? static_cast<int64_t>(num_pages) * Hkv * page_size
+                                         : static_cast<int64_t>(B) * Hkv * Lmax;
   const int64_t tree_rows = static_cast<int64_t>(B) * Hkv * n;
-  if (!make_kv_map(&maps[0], k_cache, cache_rows > 0 ? cache_rows : 1, dh, p.NK) ||
-      !make_kv_map(&maps[1], v_cache, cache_rows > 0 ? cache_rows : 1, dh, p.NK) ||
+  if (!make_kv_map(&maps[0], k_cache, cache_rows > 0 ? cache_rows : 1, dh, page_box) ||
+      !make_kv_map(&maps[1], v_cache, cache_rows > 0 ? cache_rows : 1, dh, page_box) ||
       !make_kv_map(&maps[2], k_tree, tree_rows, dh, p.NK) || !make_kv_map(&maps[3], v_tree, tree_rows, dh, p.NK))
     return cudaErrorInvalidValue;
   TcArgs a;
@@ -568,6 +608,8 @@ cudaError_t launch_tree_attn_tc(const void *q, const void *k_cache, const void *
   a.mask = mask;
   a.B = B; a.n = n; a.Hq = Hq; a.Hkv = Hkv; a.G = Hq / Hkv; a.Lmax = Lmax; a.S = p.S;
   a.W = (n + 63) / 64;
+  a.block_table = block_table;
+  a.max_pages = max_pages; a.page_size = page_size; a.page_box = page_box; a.num_pages = num_pages;
   a.scale_log2 = scale * kLog2e;
   a.out = reinterpret_cast<__nv_bfloat16 *>(out);
   a.lse = lse;
@@ -583,6 +625,25 @@ cudaError_t launch_tree_attn_tc(const void *q, const void *k_cache, const void *
   }
   if (e != cudaSuccess || p.S == 1) return e;
   return launch_attn_combine_bf16(a.part_o, a.part_ml, B, n, Hq, dh, p.S, out, lse, st);
+}
+
+cudaError_t launch_tree_attn_tc(const void *q, const void *k_cache, const void *v_cache, const int32_t *kv_len,
+                                const void *k_tree, const void *v_tree, const uint64_t *mask, int B, int n,
+                                int Hq, int Hkv, int dh, int Lmax, float scale, void *out, float *lse, void *ws,
+                                int32_t *status, int num_sms, cudaStream_t st) {
+  return launch_tc_common(q, k_cache, v_cache, kv_len, k_tree, v_tree, mask, B, n, Hq, Hkv, dh, Lmax, scale, out,
+                          lse, ws, status, num_sms, st, nullptr, 0, 0, 0);
+}
+
+cudaError_t launch_tree_attn_tc_paged(const void *q, const void *k_pages, const void *v_pages,
+                                      const int32_t *block_table, int max_pages, int page_size, int num_pages,
+                                      const int32_t *kv_len, const void *k_tree, const void *v_tree,
+                                      const uint64_t *mask, int B, int n, int Hq, int Hkv, int dh, float scale,
+                                      void *out, float *lse, void *ws, int32_t *status, int num_sms,
+                                      cudaStream_t st) {
+  return launch_tc_common(q, k_pages, v_pages, kv_len, k_tree, v_tree, mask, B, n, Hq, Hkv, dh,
+                          max_pages * page_size, scale, out, lse, ws, status, num_sms, st, block_table, max_pages,
+                          page_size, num_pages);
 }
 
 }  // namespace eagle
