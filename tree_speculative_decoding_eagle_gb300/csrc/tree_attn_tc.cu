@@ -53,6 +53,8 @@ struct TcArgs {
   __nv_bfloat16 *out;
   float *lse;
   float *part_o, *part_ml;
+  uint32_t *tickets;  // split merge: one counter per (b, g, M-group), reset by the last CTA
+  int q_tma;          // 1: Q tiles arrive by TMA (128 % G == 0), else plain loads
   int32_t *status;
 };
 
@@ -63,7 +65,7 @@ struct TcShape {
   static constexpr int kTileBytes = kRegions * NK * 128;     // one K (or V) tile
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kBarOff = kQBytes + STAGES * kStageBytes;
-  static constexpr int kNumBars = 2 * STAGES + 4 * MT + 3;
+  static constexpr int kNumBars = 2 * STAGES + 4 * MT + 4;
   static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;  // + alignment slack
   static constexpr int kThreads = MT * 128 + 64;
   static constexpr int kColS = 0;                            // S_t at t*NK
@@ -78,7 +80,7 @@ template <int DH, int MT, int NK, int STAGES>
 __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
     tree_attn_tc_kernel(const __grid_constant__ CUtensorMap kc_map, const __grid_constant__ CUtensorMap vc_map,
                         const __grid_constant__ CUtensorMap kt_map, const __grid_constant__ CUtensorMap vt_map,
-                        TcArgs a) {
+                        const __grid_constant__ CUtensorMap q_map, TcArgs a) {
   using Sh = TcShape<DH, MT, NK, STAGES>;
   constexpr int NH = NK / 64;  // 64-key halves of a tile
   extern __shared__ unsigned char raw_smem[];
@@ -95,6 +97,7 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
   uint64_t *o_done = p_full + MT;
   uint64_t *teardown = o_done + MT;
   uint64_t *turn = teardown + 1;  // exponent-pass token of M-tile 0 / 1
+  uint64_t *q_full = turn + 2;    // the Q tiles (TMA)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Sh::kNumBars);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -111,9 +114,14 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
   const int T = np + ntt;  // key tiles of this CTA
   const int producer_warp = MT * 4, mma_warp = MT * 4 + 1;
 
-  // ---- Q tiles -> shared memory (zero rows beyond the last node) ----------
+  // ---- Q tiles -> shared memory ---------------------------------------------
+  // By TMA when the group size divides 128: a box of (64 columns, G heads,
+  // 128/G nodes) lands as 128 rows in (node, grouped head) order, the M-tile
+  // row order; rows past the batch are zero-filled, rows past this
+  // sequence's last node hold the next sequence's queries (their outputs
+  // are never written).  Otherwise plain loads with zero rows.
   const int rows_total = n * a.G;
-  for (int idx = tid; idx < MT * 128 * (DH / 8); idx += Sh::kThreads) {
+  for (int idx = tid; !a.q_tma && idx < MT * 128 * (DH / 8); idx += Sh::kThreads) {
     const int t = idx / (128 * (DH / 8));
     const int rem = idx % (128 * (DH / 8));
     const int r = rem / (DH / 8), c = rem % (DH / 8);
@@ -141,6 +149,7 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
     mbar_init(teardown, 1);
     mbar_init(&turn[0], 4);
     mbar_init(&turn[1], 4);
+    mbar_init(q_full, 1);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -158,6 +167,14 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
   if (warp == producer_warp) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
+      if (a.q_tma) {
+        mbar_arrive_expect_tx(q_full, MT * Sh::kRegions * 16384);
+        for (int t = 0; t < MT; ++t)
+#pragma unroll
+          for (int r = 0; r < Sh::kRegions; ++r)
+            tma_load_3d(sQ + (t * Sh::kRegions + r) * 16384, &q_map, r * 64, g * a.G,
+                        b * n + (mg * MT + t) * (128 / a.G), q_full);
+      }
       prefetch_tmap(&kc_map);
       prefetch_tmap(&vc_map);
       prefetch_tmap(&kt_map);
@@ -250,7 +267,7 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
         }
         mma_commit(&s_full[t]);
       };
-      bool ok = T == 0 || mbar_wait(&kv_full[0], 0, abort_flag);
+      bool ok = T == 0 || ((!a.q_tma || mbar_wait(q_full, 0, abort_flag)) && mbar_wait(&kv_full[0], 0, abort_flag));
       if (ok && T > 0) {
         tc_fence_after();
         for (int t = 0; t < MT; ++t) issue_s(0, t);
@@ -479,12 +496,78 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
     }
     if (warp == producer_warp && lane == 0) {
       // copies still in flight complete before shared memory is released
+      if (a.q_tma) mbar_wait(q_full, 0, &never, 100000000ull);
       for (int j = max(0, issued - STAGES); j < issued; ++j)
         mbar_wait(&kv_full[j % STAGES], (j / STAGES) & 1, &never, 100000000ull);
     }
     __syncthreads();
   }
   if (warp == mma_warp) tmem_dealloc(tmem, Sh::kTmemCols);
+
+  // ---- split merge: the last CTA of this (b, g, M-group) combines the S
+  // partial results (max m, sum l, unnormalised O) of its rows ------------
+  if (a.S > 1) {
+    __shared__ int s_is_last;
+    __threadfence();  // this CTA's partials are visible before its ticket
+    __syncthreads();
+    if (tid == 0) {
+      const int idx = bg * gridDim.y + mg;
+      const uint32_t old = atomicAdd(&a.tickets[idx], 1u);
+      s_is_last = old == static_cast<uint32_t>(a.S - 1);
+      if (s_is_last) a.tickets[idx] = 0;  // every split has arrived: ready for the next call
+    }
+    __syncthreads();
+    if (s_is_last) {
+      __threadfence();
+      // (1) per row: the splits' weights exp(m_s - M) / L into shared memory
+      // (the stage buffers, all copies done), and the row's lse
+      const int r0 = mg * MT * 128, nr = max(0, min(rows_total, r0 + MT * 128) - r0);
+      float *s_w = reinterpret_cast<float *>(sKV);  // [nr][S]
+      for (int rr = tid; rr < nr; rr += Sh::kThreads) {
+        const int rho = r0 + rr, i = rho / a.G, h = g * a.G + rho % a.G;
+        const int64_t base = ((static_cast<int64_t>(b) * a.Hq + h) * a.S) * n + i;
+        float M = -INFINITY;
+#pragma unroll 8
+        for (int sp = 0; sp < a.S; ++sp) M = fmaxf(M, a.part_ml[(base + static_cast<int64_t>(sp) * n) * 2]);
+        float Ls = 0.f;
+#pragma unroll 8
+        for (int sp = 0; sp < a.S; ++sp) {
+          const int64_t pr = base + static_cast<int64_t>(sp) * n;
+          const float ms = a.part_ml[pr * 2];
+          const float wgt = (M > -INFINITY && ms > -INFINITY) ? ex2_approx((ms - M) * kLog2e) : 0.f;
+          Ls += wgt * a.part_ml[pr * 2 + 1];
+          s_w[rr * a.S + sp] = wgt;
+        }
+        const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+        for (int sp = 0; sp < a.S; ++sp) s_w[rr * a.S + sp] *= inv;
+        if (a.lse) a.lse[(static_cast<int64_t>(b) * n + i) * a.Hq + h] = Ls > 0.f ? M + __logf(Ls) : -INFINITY;
+      }
+      __syncthreads();
+      // (2) out = sum_s w_s O_s, four columns per item
+      constexpr int NV = DH / 4;
+      for (int item = tid; item < nr * NV; item += Sh::kThreads) {
+        const int rr = item / NV, c = item % NV;
+        const int rho = r0 + rr, i = rho / a.G, h = g * a.G + rho % a.G;
+        const int64_t base = ((static_cast<int64_t>(b) * a.Hq + h) * a.S) * n + i;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int sp = 0; sp < a.S; ++sp) {
+          const float wgt = s_w[rr * a.S + sp];
+          if (wgt != 0.f) {
+            const float4 po = reinterpret_cast<const float4 *>(a.part_o + (base + static_cast<int64_t>(sp) * n) * DH)[c];
+            o.x += wgt * po.x; o.y += wgt * po.y; o.z += wgt * po.z; o.w += wgt * po.w;
+          }
+        }
+        const int64_t orow = (static_cast<int64_t>(b) * n + i) * a.Hq + h;
+        __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(o.z, o.w);
+        uint2 packed;
+        packed.x = *reinterpret_cast<const uint32_t *>(&lo);
+        packed.y = *reinterpret_cast<const uint32_t *>(&hi);
+        reinterpret_cast<uint2 *>(a.out + orow * DH)[c] = packed;
+      }
+    }
+  }
 }
 
 // ---- host side ---------------------------------------------------------------
@@ -517,6 +600,20 @@ static bool make_kv_map(CUtensorMap *map, const void *base, int64_t rows, int dh
   cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Q [B*n, Hq, dh] bf16 viewed as a 3D tensor with boxes of 64 columns x G
+// heads x 128/G nodes (128-byte swizzle): one box is one M-tile region.
+static bool make_q_map(CUtensorMap *map, const void *base, int64_t rows, int Hq, int dh, int G) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(dh), static_cast<cuuint64_t>(Hq), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(dh) * 2, static_cast<cuuint64_t>(Hq) * dh * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(128 / G)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -555,14 +652,14 @@ static TcPlan tc_plan(int B, int n, int Hq, int Hkv, int dh, int Lmax, int num_s
   return p;
 }
 
+// Split workspace: fp32 partial O [B, Hq, S, n, dh], (m, l) [B, Hq, S, n, 2],
+// then one merge ticket per (b, g, M-group).
 size_t attn_tc_workspace_bytes(int B, int n, int Hq, int Hkv, int dh, int Lmax, int num_sms) {
   const TcPlan p = tc_plan(B, n, Hq, Hkv, dh, Lmax, num_sms);
   if (p.S == 1) return 0;
-  return sizeof(float) * static_cast<size_t>(B) * Hq * p.S * n * (dh + 2);
+  return sizeof(float) * static_cast<size_t>(B) * Hq * p.S * n * (dh + 2) +
+         sizeof(uint32_t) * static_cast<size_t>(B) * Hkv * p.mgroups;
 }
-
-cudaError_t launch_attn_combine_bf16(const float *part_o, const float *part_ml, int B, int n, int Hq, int dh,
-                                     int S, void *out, float *lse, cudaStream_t st);
 
 template <int DH, int MT, int NK, int STAGES>
 static cudaError_t launch_tc_t(const CUtensorMap *maps, const TcArgs &a, const TcPlan &p, cudaStream_t st) {
@@ -579,7 +676,7 @@ static cudaError_t launch_tc_t(const CUtensorMap *maps, const TcArgs &a, const T
   }
   dim3 grid(p.S, p.mgroups, a.B * a.Hkv);
   tree_attn_tc_kernel<DH, MT, NK, STAGES><<<grid, Sh::kThreads, Sh::kSmem, st>>>(maps[0], maps[1], maps[2],
-                                                                                maps[3], a);
+                                                                                maps[3], maps[4], a);
   return cudaGetLastError();
 }
 
@@ -591,7 +688,7 @@ static cudaError_t launch_tc_common(const void *q, const void *k_cache, const vo
                                     void *ws, int32_t *status, int num_sms, cudaStream_t st,
                                     const int32_t *block_table, int max_pages, int page_size, int num_pages) {
   const TcPlan p = tc_plan(B, n, Hq, Hkv, dh, Lmax, num_sms);
-  CUtensorMap maps[4];
+  CUtensorMap maps[5];
   const int page_box = block_table ? min(page_size, p.NK) : p.NK;
   const int64_t cache_rows = block_table ? static_cast<int64_t>(num_pages) * Hkv * page_size
                                          : static_cast<int64_t>(B) * Hkv * Lmax;
@@ -600,6 +697,9 @@ static cudaError_t launch_tc_common(const void *q, const void *k_cache, const vo
       !make_kv_map(&maps[1], v_cache, cache_rows > 0 ? cache_rows : 1, dh, page_box) ||
       !make_kv_map(&maps[2], k_tree, tree_rows, dh, p.NK) || !make_kv_map(&maps[3], v_tree, tree_rows, dh, p.NK))
     return cudaErrorInvalidValue;
+  const int G = Hq / Hkv;
+  const bool q_tma = 128 % G == 0 && make_q_map(&maps[4], q, static_cast<int64_t>(B) * n, Hq, dh, G);
+  if (!q_tma) maps[4] = maps[2];  // unused
   TcArgs a;
   a.q = reinterpret_cast<const __nv_bfloat16 *>(q);
   a.k_cache = reinterpret_cast<const __nv_bfloat16 *>(k_cache);
@@ -615,6 +715,8 @@ static cudaError_t launch_tc_common(const void *q, const void *k_cache, const vo
   a.lse = lse;
   a.part_o = reinterpret_cast<float *>(ws);
   a.part_ml = a.part_o + static_cast<size_t>(B) * Hq * p.S * n * dh;
+  a.tickets = reinterpret_cast<uint32_t *>(a.part_ml + static_cast<size_t>(B) * Hq * p.S * n * 2);
+  a.q_tma = q_tma ? 1 : 0;
   a.status = status;
   cudaError_t e;
   // stages: as many as shared memory allows at the variant's CTAs per SM
@@ -623,8 +725,7 @@ static cudaError_t launch_tc_common(const void *q, const void *k_cache, const vo
   } else {
     e = p.MT == 1 ? launch_tc_t<128, 1, 64, 2>(maps, a, p, st) : launch_tc_t<128, 2, 64, 4>(maps, a, p, st);
   }
-  if (e != cudaSuccess || p.S == 1) return e;
-  return launch_attn_combine_bf16(a.part_o, a.part_ml, B, n, Hq, dh, p.S, out, lse, st);
+  return e;
 }
 
 cudaError_t launch_tree_attn_tc(const void *q, const void *k_cache, const void *v_cache, const int32_t *kv_len,
