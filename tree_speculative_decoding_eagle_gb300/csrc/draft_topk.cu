@@ -68,23 +68,22 @@ __device__ __forceinline__ int rank_in(uint64_t key, const uint64_t *set, int n)
   return r;
 }
 
-// The warp's k best of its list wl[0..*wn) and its buffer buf[0..fill),
-// written back to wl in descending order (whole warp, rank by counting).
-__device__ __forceinline__ void warp_compact(uint64_t *wl, int *wn, uint64_t *buf, int fill, uint64_t *tmp,
-                                             int k, int lane) {
-  __syncwarp();
-  const int n0 = *wn;
-  const int C = n0 + fill;
-  for (int i = lane; i < C; i += 32) {
-    const uint64_t key = i < n0 ? wl[i] : buf[i - n0];
-    const int r = rank_in(key, wl, n0) + rank_in(key, buf, fill);
-    if (r < k) tmp[r] = key;
-  }
-  __syncwarp();
-  const int nk = C < k ? C : k;
-  if (lane < nk) wl[lane] = tmp[lane];
-  if (lane == 0) *wn = nk;
-  __syncwarp();
+__device__ __forceinline__ uint64_t shfl_up_u64(uint64_t v, int d) {
+  uint32_t lo = static_cast<uint32_t>(v), hi = static_cast<uint32_t>(v >> 32);
+  lo = __shfl_up_sync(0xffffffffu, lo, d);
+  hi = __shfl_up_sync(0xffffffffu, hi, d);
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
+// Element e of a 16-byte vector as float (no indexed register access).
+template <typename T> __device__ __forceinline__ float elem_of(const uint4 &v, int e);
+template <> __device__ __forceinline__ float elem_of<__nv_bfloat16>(const uint4 &v, int e) {
+  const int q = e >> 1;
+  const uint32_t w = q == 0 ? v.x : (q == 1 ? v.y : (q == 2 ? v.z : v.w));
+  return (e & 1) ? bf16_hi(w) : bf16_lo(w);
+}
+template <> __device__ __forceinline__ float elem_of<float>(const uint4 &v, int e) {
+  return __uint_as_float(e == 0 ? v.x : (e == 1 ? v.y : (e == 2 ? v.z : v.w)));
 }
 
 template <typename T>
@@ -93,10 +92,9 @@ __global__ void __launch_bounds__(kDraftThreads, 3) draft_topk_kernel(DraftArgs 
   constexpr int VEC = VT::kElems;
   constexpr int NVL = kDraftVecPerLane;
   constexpr int SEG = 32 * NVL * VEC;  // tokens per warp
-  constexpr int CAP = 32 * VEC;        // candidate buffer per warp (one full vector step)
   constexpr int NW = kDraftThreads / 32;
-  __shared__ uint64_t s_buf[NW][CAP];
-  __shared__ uint64_t s_wl[NW][32], s_tmp[NW][32];
+  __shared__ uint64_t s_buf[NW][32 * 4];  // gathered keys of the block merge (NW*k, or S*k in the split merge)
+  __shared__ uint64_t s_wl[NW][32];
   __shared__ int s_wn[NW];
   __shared__ uint64_t s_top[32];
   __shared__ float s_m[NW], s_s[NW];
@@ -110,8 +108,6 @@ __global__ void __launch_bounds__(kDraftThreads, 3) draft_topk_kernel(DraftArgs 
   const int j = r == 0 ? 0 : (r - 1) % a.k;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = a.k;
-  uint64_t *buf = s_buf[warp];
-  uint64_t *wl = s_wl[warp];
 
   const T *row = reinterpret_cast<const T *>(a.logits) +
                  ((static_cast<int64_t>(b) * a.D + d) * a.k + j) * a.ld;
@@ -128,7 +124,22 @@ __global__ void __launch_bounds__(kDraftThreads, 3) draft_topk_kernel(DraftArgs 
   float m = -INFINITY, sum = 0.f;  // this lane's running max and sum of exp(x - m)
   float lmax = -INFINITY;          // this lane's largest value so far
   float thr = -INFINITY;           // prune bound: at least k values of the part are >= thr
-  int fill = 0;
+  float published = -INFINITY;     // this warp's bound as last raised in s_thr
+  // The warp's top keys so far, sorted, in registers: lane i < k holds the
+  // i-th (0 = empty); cnt of them are set (warp-uniform).  Once k are set,
+  // lane k-1's key is the tightest prune bound.
+  uint64_t mine = 0;
+  int cnt = 0;
+  auto insert = [&](uint64_t key) {  // called by the whole warp with one key
+    const int pos = __popc(__ballot_sync(0xffffffffu, lane < k && mine > key));
+    if (pos < k) {
+      const uint64_t up = shfl_up_u64(mine, 1);
+      if (lane > pos && lane < k) mine = up;
+      if (lane == pos) mine = key;
+      cnt = cnt < k ? cnt + 1 : k;
+      if (cnt == k) thr = fmaxf(thr, key_value(shfl_u64(mine, k - 1)));
+    }
+  };
   for (int gseg = g0 + warp; gseg < g1; gseg += NW) {
     const int seg0 = gseg * SEG;
     const int nvec = min(SEG, a.V - seg0) / VEC;
@@ -146,63 +157,66 @@ __global__ void __launch_bounds__(kDraftThreads, 3) draft_topk_kernel(DraftArgs 
       smax = fmaxf(smax, vmx[i]);
     }
     if (smax > -INFINITY) {
-      const float mL = smax * kLog2e;
-      const uint64_t L2 = f2_pack(kLog2e, kLog2e), nmL2 = f2_pack(-mL, -mL);
-      uint64_t acc = f2_pack(0.f, 0.f);
+      // sum of 2^(x*log2e - smax*log2e): per element one extract, FMA, ex2, add
+      const float nmL = -smax * kLog2e;
+      float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-      for (int i = 0; i < NVL; ++i)
-        if (lane + 32 * i < nvec) acc = vec_exp_sum<T>(vb[i], L2, nmL2, acc);
-      float a0, a1;
-      f2_unpack(acc, a0, a1);
-      lse_combine(m, sum, smax, a0 + a1);
+      for (int i = 0; i < NVL; ++i) {
+        if (lane + 32 * i < nvec) {
+          float x[VEC];
+          VT::unpack(vb[i], x);
+#pragma unroll
+          for (int e = 0; e < VEC; e += 2) {
+            acc0 += ex2_approx(fmaf(x[e], kLog2e, nmL));
+            acc1 += ex2_approx(fmaf(x[e + 1], kLog2e, nmL));
+          }
+        }
+      }
+      lse_combine(m, sum, smax, acc0 + acc1);
     }
     lmax = fmaxf(lmax, smax);
-    // Lane maxima are distinct elements, so the k-th largest lane maximum of
-    // the warp has at least k elements at or above it; the k-th key of a full
-    // warp list too.  The block keeps the largest such bound.
-    {
+    // prune bound: before the list holds k keys, the k-th largest lane
+    // maximum (lane maxima are distinct elements); the block's shared
+    // maximum of its warps' bounds every segment (one shared load)
+    if (cnt < k) {
       const float y = warp_sort_desc(lmax, lane);
-      float tw = __shfl_sync(0xffffffffu, y, k - 1);
-      if (s_wn[warp] == k) tw = fmaxf(tw, key_value(wl[k - 1]));
-      if (lane == 0 && tw > -INFINITY) atomicMax(&s_thr, ordered_u32(tw));
-      thr = fmaxf(thr, fmaxf(tw, from_ordered_u32(*const_cast<volatile unsigned *>(&s_thr))));
+      thr = fmaxf(thr, __shfl_sync(0xffffffffu, y, k - 1));
     }
+    thr = fmaxf(thr, from_ordered_u32(*const_cast<volatile unsigned *>(&s_thr)));
+    if (!__any_sync(0xffffffffu, smax > -INFINITY && smax >= thr)) continue;
 #pragma unroll
     for (int i = 0; i < NVL; ++i) {
-      const bool maybe = vmx[i] > -INFINITY && vmx[i] >= thr;
-      if (__any_sync(0xffffffffu, maybe)) {
-        unsigned cm = 0;
+      unsigned cm = 0;  // this lane's elements of vector i at or above the bound
+      if (vmx[i] > -INFINITY && vmx[i] >= thr) {
         float x[VEC];
         VT::unpack(vb[i], x);
-        if (maybe) {
 #pragma unroll
-          for (int e = 0; e < VEC; ++e)
-            if (x[e] >= thr && x[e] > -INFINITY) cm |= 1u << e;
+        for (int e = 0; e < VEC; ++e)
+          if (x[e] >= thr && x[e] > -INFINITY) cm |= 1u << e;
+      }
+      // insert them one by one (lowest lane, lowest element first); each
+      // insert may raise the bound and drop later ones
+      for (unsigned lanes = __ballot_sync(0xffffffffu, cm != 0); lanes;
+           lanes = __ballot_sync(0xffffffffu, cm != 0)) {
+        const int src = __ffs(lanes) - 1;
+        uint64_t key = 0;
+        if (lane == src) {
+          const int e = __ffs(cm) - 1;
+          cm &= cm - 1;
+          key = topk_key(elem_of<T>(vb[i], e), static_cast<uint32_t>(seg0 + (lane + 32 * i) * VEC + e));
         }
-        const int cnt = __popc(cm);
-        int incl = cnt;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int v = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += v;
-        }
-        const int total = __shfl_sync(0xffffffffu, incl, 31);
-        if (fill + total > CAP) {
-          warp_compact(wl, &s_wn[warp], buf, fill, s_tmp[warp], k, lane);
-          fill = 0;
-        }
-        if (cm) {
-          int pos = fill + incl - cnt;
-          const uint32_t t0 = static_cast<uint32_t>(seg0 + (lane + 32 * i) * VEC);
-#pragma unroll
-          for (int e = 0; e < VEC; ++e)
-            if ((cm >> e) & 1u) buf[pos++] = topk_key(x[e], t0 + e);
-        }
-        fill += total;
+        key = shfl_u64(key, src);
+        if (key_value(key) >= thr) insert(key);
+        if (cm && !(vmx[i] >= thr)) cm = 0;  // the raised bound excludes the rest of this vector
       }
     }
+    if (cnt == k && thr > published) {  // raise the block's bound (rare once warm)
+      if (lane == 0) atomicMax(&s_thr, ordered_u32(thr));
+      published = thr;
+    }
   }
-  if (fill > 0) warp_compact(wl, &s_wn[warp], buf, fill, s_tmp[warp], k, lane);
+  if (lane < k) s_wl[warp][lane] = mine;
+  if (lane == 0) s_wn[warp] = cnt;
 
   // ---- block: softmax statistics and the top k of the warp lists ------------
   {
