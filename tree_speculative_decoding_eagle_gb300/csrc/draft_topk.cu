@@ -6,19 +6,19 @@
 // token id) and c = exp(x - M) / Z.
 //
 // One pass over HBM.  A row is split into parts of 8 warps x 2048 tokens
-// (bf16; 1024 for fp32), one CTA per part.  Each warp holds its segment in
-// registers (all 16-byte loads in flight at once) and takes two passes over
-// them: lane maxima, then the sum of exp(x - lane max).  Top-k selection works on unique 64-bit keys (logit order, then
-// lower token id).  Every lane tracks its running maximum; the k-th largest
-// lane maximum of a warp (a 32-lane bitonic sort per chunk) bounds the top k
-// from below, and the block keeps the largest such bound.  Values at or
-// above the bound are appended to a per-warp shared-memory buffer by a
-// ballot scan, so only about k candidates per warp survive.  Merges keep the
-// code small: the k best of a set of unique keys are found by counting, for
-// each key, how many keys are larger (its rank), in shared memory.  Warp lists
-// merge block-wide through shared memory.  With S > 1 the last CTA of a row
-// to finish (atomic ticket in the workspace) merges the S partial results;
-// no CTA ever waits for another.
+// (bf16; 1024 for fp32), one CTA per part.  Each warp holds a segment in
+// registers (all 16-byte loads in flight at once) and visits it twice: lane
+// maxima, then the sum of exp(x - segment max), folded into a running
+// (max, sum).  Top-k selection works on unique 64-bit keys (logit order,
+// then lower token id).  Each warp keeps its k best keys so far sorted in
+// registers (lane i holds the i-th); a new key's place is the number of
+// larger keys (one ballot) and the tail shifts down one lane.  The list's
+// k-th key bounds the part from below, so values under the bound (shared
+// block-wide as a maximum over the warps) are never looked at; before the
+// list is full, the k-th largest lane maximum is the bound.  The warp lists
+// merge block-wide by rank counting in shared memory.  With S > 1 the last
+// CTA of a row to finish (atomic ticket in the workspace) merges the S
+// partial results; no CTA ever waits for another.
 #include "common.cuh"
 
 namespace eagle {
