@@ -62,47 +62,56 @@ __global__ void __launch_bounds__(256) verify_stats_kernel(VerifyArgs a) {
       const int v = lane + 32 * i;
       if (v < nvec) buf[i] = ld_stream16(p + t_begin + v * VEC);
     }
-    float best = -INFINITY;
-    int arg = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < NVL; ++i) {
-      const int v = lane + 32 * i;
-      if (v < nvec) {
-        float x[VEC];
-        VT::unpack(buf[i], x);
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-          const float y = SAMPLE ? x[e] * a.inv_t : x[e];
-          if (y > best) {  // strict: first occurrence within the lane
-            best = y;
-            arg = t_begin + v * VEC + e;
-          }
-        }
-      }
-    }
-    const uint32_t om = __reduce_max_sync(0xffffffffu, ordered_u32(best));
-    const float M = from_ordered_u32(om);
     ChunkStat st;
-    st.m = M;
     st.pad = 0;
     if (SAMPLE) {
-      float s = 0.f;
+      // max of the raw logits (packed max; scaling by 1/T > 0 keeps order,
+      // so the chunk max of x/T is max(x) / T exactly), then
+      // sum exp(x/T - M) with 1/T folded into the exponent's FMA
+      float bx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < NVL; ++i)
+        if (lane + 32 * i < nvec) bx = fmaxf(bx, vec_max<T>(buf[i]));
+      const float M = from_ordered_u32(__reduce_max_sync(0xffffffffu, ordered_u32(bx))) * a.inv_t;
+      float s0 = 0.f, s1 = 0.f;
       if (M > -INFINITY) {
-        const float mL = M * kLog2e;
+        const float sc = a.inv_t * kLog2e, nmL = -M * kLog2e;
 #pragma unroll
         for (int i = 0; i < NVL; ++i) {
-          const int v = lane + 32 * i;
-          if (v < nvec) {
+          if (lane + 32 * i < nvec) {
             float x[VEC];
             VT::unpack(buf[i], x);
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) s += ex2_approx(fmaf(x[e] * a.inv_t, kLog2e, -mL));
+            for (int e = 0; e < VEC; e += 2) {
+              s0 += ex2_approx(fmaf(x[e], sc, nmL));
+              s1 += ex2_approx(fmaf(x[e + 1], sc, nmL));
+            }
           }
         }
       }
-      st.s = warp_sum(s);
+      st.m = M;
+      st.s = warp_sum(s0 + s1);
       st.a = -1;
     } else {
+      float best = -INFINITY;
+      int arg = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < NVL; ++i) {
+        const int v = lane + 32 * i;
+        if (v < nvec) {
+          float x[VEC];
+          VT::unpack(buf[i], x);
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) {
+            if (x[e] > best) {  // strict: first occurrence within the lane
+              best = x[e];
+              arg = t_begin + v * VEC + e;
+            }
+          }
+        }
+      }
+      const uint32_t om = __reduce_max_sync(0xffffffffu, ordered_u32(best));
+      st.m = from_ordered_u32(om);
       const uint32_t cand = (ordered_u32(best) == om) ? static_cast<uint32_t>(arg) : 0xffffffffu;
       st.a = static_cast<int>(__reduce_min_sync(0xffffffffu, cand));
       st.s = 0.f;
@@ -127,6 +136,7 @@ __global__ void __launch_bounds__(32) verify_walk_kernel(VerifyArgs a) {
   const int lane = threadIdx.x;
   const int n = a.n;
   const int64_t nb = static_cast<int64_t>(b) * n;
+  const float sc = a.inv_t * kLog2e;  // logit -> base-2 exponent of exp(x / T), as the statistics pass
   for (int i = lane; i < n; i += 32) {
     s_par[i] = a.node_parent[nb + i];
     s_tok[i] = a.node_tok[nb + i];
@@ -177,7 +187,7 @@ __global__ void __launch_bounds__(32) verify_walk_kernel(VerifyArgs a) {
           const int t = s_tok[x];
           const bool t_ok = t >= 0 && t < a.V;
           if (!t_ok && lane == 0) report(a.status, EAGLE_ERR_INVALID);
-          const float e = t_ok ? ex2_approx(fmaf(logit_at<T>(a, row, t) * a.inv_t, kLog2e, -mL)) : 0.f;
+          const float e = t_ok ? ex2_approx(fmaf(logit_at<T>(a, row, t), sc, -mL)) : 0.f;
           const float u0 = a.u[(nb + x) * 2 + 0];
           if (u0 * (Z - rej_sum) < e) {
             next = x;
@@ -203,7 +213,7 @@ __global__ void __launch_bounds__(32) verify_walk_kernel(VerifyArgs a) {
           float w = st.m > -INFINITY ? st.s * ex2_approx(fmaf(st.m, kLog2e, -mL)) : 0.f;
           for (int q = 0; q < n_rej; ++q) {
             const int t = s_rej[q];
-            if (t >= 0 && t / kChunk == c) w -= ex2_approx(fmaf(logit_at<T>(a, row, t) * a.inv_t, kLog2e, -mL));
+            if (t >= 0 && t / kChunk == c) w -= ex2_approx(fmaf(logit_at<T>(a, row, t), sc, -mL));
           }
           lane_mass += fmaxf(w, 0.f);
         }
@@ -231,7 +241,7 @@ __global__ void __launch_bounds__(32) verify_walk_kernel(VerifyArgs a) {
             float w = st.m > -INFINITY ? st.s * ex2_approx(fmaf(st.m, kLog2e, -mL)) : 0.f;
             for (int q = 0; q < n_rej; ++q) {
               const int t = s_rej[q];
-              if (t >= 0 && t / kChunk == c) w -= ex2_approx(fmaf(logit_at<T>(a, row, t) * a.inv_t, kLog2e, -mL));
+              if (t >= 0 && t / kChunk == c) w -= ex2_approx(fmaf(logit_at<T>(a, row, t), sc, -mL));
             }
             w = fmaxf(w, 0.f);
             if (w > 0.f) { lastnz = c; lastbefore = run; }
@@ -253,7 +263,7 @@ __global__ void __launch_bounds__(32) verify_walk_kernel(VerifyArgs a) {
         for (int t = tb; t < te; ++t) {
           bool in_s = false;
           for (int q = 0; q < n_rej; ++q) in_s |= (s_rej[q] == t);
-          if (!in_s) lane_w += ex2_approx(fmaf(logit_at<T>(a, row, t) * a.inv_t, kLog2e, -mL));
+          if (!in_s) lane_w += ex2_approx(fmaf(logit_at<T>(a, row, t), sc, -mL));
         }
         double lincl = lane_w;
 #pragma unroll
@@ -274,7 +284,7 @@ __global__ void __launch_bounds__(32) verify_walk_kernel(VerifyArgs a) {
             bool in_s = false;
             for (int q = 0; q < n_rej; ++q) in_s |= (s_rej[q] == t);
             if (in_s) continue;
-            const float w = ex2_approx(fmaf(logit_at<T>(a, row, t) * a.inv_t, kLog2e, -mL));
+            const float w = ex2_approx(fmaf(logit_at<T>(a, row, t), sc, -mL));
             if (w > 0.f) lastnz = t;
             run += w;
             if (run > tgt && w > 0.f) { tok = t; break; }
