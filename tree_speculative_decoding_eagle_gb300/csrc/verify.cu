@@ -132,6 +132,7 @@ __global__ void __launch_bounds__(32) verify_walk_kernel(VerifyArgs a) {
   int *s_par = reinterpret_cast<int *>(smem);
   int *s_tok = s_par + a.n;
   int *s_rej = s_tok + a.n;  // rejected tokens at the current node
+  float *s_rej_e = reinterpret_cast<float *>(s_rej + a.n);  // and their exp terms
   const int b = blockIdx.x;
   const int lane = threadIdx.x;
   const int n = a.n;
@@ -179,21 +180,34 @@ __global__ void __launch_bounds__(32) verify_walk_kernel(VerifyArgs a) {
       }
       Z = warp_sum(z);
       for (int base = 0; base < n && next < 0; base += 32) {
+        // the children among nodes base..base+31: each lane fetches its
+        // child's logit and uniform at once, then the decisions are taken
+        // in node order from registers
         const int i = base + lane;
-        unsigned bal = __ballot_sync(0xffffffffu, i < n && s_par[i] == cur);
+        const bool kid = i < n && s_par[i] == cur;
+        int t_l = -1;
+        float e_l = 0.f, u_l = 0.f;
+        if (kid) {
+          t_l = s_tok[i];
+          if (t_l >= 0 && t_l < a.V) e_l = ex2_approx(fmaf(logit_at<T>(a, row, t_l), sc, -mL));
+          else report(a.status, EAGLE_ERR_INVALID);
+          u_l = a.u[(nb + i) * 2 + 0];
+        }
+        unsigned bal = __ballot_sync(0xffffffffu, kid);
         while (bal && next < 0) {
-          const int x = base + __ffs(bal) - 1;
+          const int src = __ffs(bal) - 1;
           bal &= bal - 1;
-          const int t = s_tok[x];
-          const bool t_ok = t >= 0 && t < a.V;
-          if (!t_ok && lane == 0) report(a.status, EAGLE_ERR_INVALID);
-          const float e = t_ok ? ex2_approx(fmaf(logit_at<T>(a, row, t), sc, -mL)) : 0.f;
-          const float u0 = a.u[(nb + x) * 2 + 0];
+          const float e = __shfl_sync(0xffffffffu, e_l, src);
+          const float u0 = __shfl_sync(0xffffffffu, u_l, src);
+          const int t = __shfl_sync(0xffffffffu, t_l, src);
           if (u0 * (Z - rej_sum) < e) {
-            next = x;
+            next = base + src;
           } else {
             rej_sum += e;
-            if (lane == 0) s_rej[n_rej] = t;
+            if (lane == 0) {
+              s_rej[n_rej] = (t >= 0 && t < a.V) ? t : -1;
+              s_rej_e[n_rej] = e;
+            }
             ++n_rej;
           }
         }
@@ -213,7 +227,7 @@ __global__ void __launch_bounds__(32) verify_walk_kernel(VerifyArgs a) {
           float w = st.m > -INFINITY ? st.s * ex2_approx(fmaf(st.m, kLog2e, -mL)) : 0.f;
           for (int q = 0; q < n_rej; ++q) {
             const int t = s_rej[q];
-            if (t >= 0 && t / kChunk == c) w -= ex2_approx(fmaf(logit_at<T>(a, row, t), sc, -mL));
+            if (t >= 0 && t / kChunk == c) w -= s_rej_e[q];
           }
           lane_mass += fmaxf(w, 0.f);
         }
@@ -241,7 +255,7 @@ __global__ void __launch_bounds__(32) verify_walk_kernel(VerifyArgs a) {
             float w = st.m > -INFINITY ? st.s * ex2_approx(fmaf(st.m, kLog2e, -mL)) : 0.f;
             for (int q = 0; q < n_rej; ++q) {
               const int t = s_rej[q];
-              if (t >= 0 && t / kChunk == c) w -= ex2_approx(fmaf(logit_at<T>(a, row, t), sc, -mL));
+              if (t >= 0 && t / kChunk == c) w -= s_rej_e[q];
             }
             w = fmaxf(w, 0.f);
             if (w > 0.f) { lastnz = c; lastbefore = run; }
@@ -256,20 +270,37 @@ __global__ void __launch_bounds__(32) verify_walk_kernel(VerifyArgs a) {
           bonus = -1;
           break;
         }
-        // scan the chunk: lane l owns 64 consecutive tokens
+        // scan the chunk: lane l owns 64 consecutive tokens, loaded as
+        // 16-byte vectors into registers; rejected tokens are masked out
+        constexpr int VEC = VecTraits<T>::kElems, NV = 64 / VEC;
         const int tb = chunk * kChunk + lane * 64;
         const int te = min(a.V, tb + 64);
+        uint64_t rejm = 0;  // rejected tokens inside [tb, te)
+        for (int q = 0; q < n_rej; ++q) {
+          const int t = s_rej[q];
+          if (t >= tb && t < te) rejm |= 1ull << (t - tb);
+        }
+        uint4 v[NV];
+        const T *rp = reinterpret_cast<const T *>(a.target) + row * a.ld;
+#pragma unroll
+        for (int q = 0; q < NV; ++q)
+          if (tb + q * VEC < te) v[q] = *reinterpret_cast<const uint4 *>(rp + tb + q * VEC);
         float lane_w = 0.f;
-        for (int t = tb; t < te; ++t) {
-          bool in_s = false;
-          for (int q = 0; q < n_rej; ++q) in_s |= (s_rej[q] == t);
-          if (!in_s) lane_w += ex2_approx(fmaf(logit_at<T>(a, row, t), sc, -mL));
+#pragma unroll
+        for (int q = 0; q < NV; ++q) {
+          if (tb + q * VEC < te) {
+            float x[VEC];
+            VecTraits<T>::unpack(v[q], x);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e)
+              if (!((rejm >> (q * VEC + e)) & 1ull)) lane_w += ex2_approx(fmaf(x[e], sc, -mL));
+          }
         }
         double lincl = lane_w;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-          const double v = __shfl_up_sync(0xffffffffu, lincl, o);
-          if (lane >= o) lincl += v;
+          const double vv = __shfl_up_sync(0xffffffffu, lincl, o);
+          if (lane >= o) lincl += vv;
         }
         const double lexcl = before + (lincl - lane_w);
         lincl += before;
@@ -280,14 +311,20 @@ __global__ void __launch_bounds__(32) verify_walk_kernel(VerifyArgs a) {
         if (lane == hl2) {
           double run = lexcl;
           int lastnz = -1;
-          for (int t = tb; t < te; ++t) {
-            bool in_s = false;
-            for (int q = 0; q < n_rej; ++q) in_s |= (s_rej[q] == t);
-            if (in_s) continue;
-            const float w = ex2_approx(fmaf(logit_at<T>(a, row, t), sc, -mL));
-            if (w > 0.f) lastnz = t;
-            run += w;
-            if (run > tgt && w > 0.f) { tok = t; break; }
+#pragma unroll
+          for (int q = 0; q < NV; ++q) {
+            if (tok < 0 && tb + q * VEC < te) {
+              float x[VEC];
+              VecTraits<T>::unpack(v[q], x);
+#pragma unroll
+              for (int e = 0; e < VEC; ++e) {
+                if (tok >= 0 || ((rejm >> (q * VEC + e)) & 1ull)) continue;
+                const float w = ex2_approx(fmaf(x[e], sc, -mL));
+                if (w > 0.f) lastnz = tb + q * VEC + e;
+                run += w;
+                if (run > tgt && w > 0.f) tok = tb + q * VEC + e;
+              }
+            }
           }
           if (tok < 0) tok = lastnz;
         }
@@ -335,7 +372,7 @@ static cudaError_t launch_verify_t(const VerifyArgs &a, int num_sms, cudaStream_
     verify_stats_kernel<T, false><<<static_cast<int>(blocks), 256, 0, st>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const size_t smem = sizeof(int) * 3 * static_cast<size_t>(a.n);
+  const size_t smem = sizeof(int) * 4 * static_cast<size_t>(a.n);
   if (smem > 48 * 1024) {
     e = cudaFuncSetAttribute(verify_walk_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
