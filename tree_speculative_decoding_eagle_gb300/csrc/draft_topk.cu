@@ -35,6 +35,7 @@ struct DraftArgs {
 };
 
 constexpr int kDraftThreads = 256;
+constexpr int kBatchCap = 128;  // candidates of one segment merged as a batch (the warp's buffer)
 constexpr int kDraftVecPerLane = 8;  // 16-byte vectors each lane holds in registers
 
 // Workspace: [tickets: u32 per row][(max, sum) per row and split][k keys per
@@ -94,7 +95,7 @@ __global__ void __launch_bounds__(kDraftThreads, 3) draft_topk_kernel(DraftArgs 
   constexpr int SEG = 32 * NVL * VEC;  // tokens per warp
   constexpr int NW = kDraftThreads / 32;
   __shared__ uint64_t s_buf[NW][32 * 4];  // gathered keys of the block merge (NW*k, or S*k in the split merge)
-  __shared__ uint64_t s_wl[NW][32];
+  __shared__ uint64_t s_wl[NW][32], s_tmp[NW][32];
   __shared__ int s_wn[NW];
   __shared__ uint64_t s_top[32];
   __shared__ float s_m[NW], s_s[NW];
@@ -184,16 +185,54 @@ __global__ void __launch_bounds__(kDraftThreads, 3) draft_topk_kernel(DraftArgs 
     }
     thr = fmaxf(thr, from_ordered_u32(*const_cast<volatile unsigned *>(&s_thr)));
     if (!__any_sync(0xffffffffu, smax > -INFINITY && smax >= thr)) continue;
+    unsigned cms[NVL];  // this lane's elements of each vector at or above the bound
+    int mycnt = 0;
 #pragma unroll
     for (int i = 0; i < NVL; ++i) {
-      unsigned cm = 0;  // this lane's elements of vector i at or above the bound
+      cms[i] = 0;
       if (vmx[i] > -INFINITY && vmx[i] >= thr) {
         float x[VEC];
         VT::unpack(vb[i], x);
 #pragma unroll
         for (int e = 0; e < VEC; ++e)
-          if (x[e] >= thr && x[e] > -INFINITY) cm |= 1u << e;
+          if (x[e] >= thr && x[e] > -INFINITY) cms[i] |= 1u << e;
       }
+      mycnt += __popc(cms[i]);
+    }
+    const int total = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(mycnt)));
+    if (total > 4 && total <= kBatchCap) {
+      // many candidates (a warp's first segment): write them to the warp's
+      // buffer, then keep the k best of list + buffer by rank counting
+      int pos = mycnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, pos, o);
+        if (lane >= o) pos += v;
+      }
+      pos -= mycnt;
+      uint64_t *buf = s_buf[warp];
+#pragma unroll
+      for (int i = 0; i < NVL; ++i)
+        for (unsigned cm = cms[i]; cm; cm &= cm - 1) {
+          const int e = __ffs(cm) - 1;
+          buf[pos++] = topk_key(elem_of<T>(vb[i], e), static_cast<uint32_t>(seg0 + (lane + 32 * i) * VEC + e));
+        }
+      if (lane < cnt) s_wl[warp][lane] = mine;
+      __syncwarp();
+      for (int q = lane; q < cnt + total; q += 32) {
+        const uint64_t key = q < cnt ? s_wl[warp][q] : buf[q - cnt];
+        const int rk = rank_in(key, s_wl[warp], cnt) + rank_in(key, buf, total);
+        if (rk < k) s_tmp[warp][rk] = key;
+      }
+      __syncwarp();
+      cnt = cnt + total < k ? cnt + total : k;
+      mine = lane < cnt ? s_tmp[warp][lane] : 0ull;
+      if (cnt == k) thr = fmaxf(thr, key_value(shfl_u64(mine, k - 1)));
+      __syncwarp();
+    } else {
+#pragma unroll
+    for (int i = 0; i < NVL; ++i) {
+      unsigned cm = cms[i];
       // insert them one by one (lowest lane, lowest element first); each
       // insert may raise the bound and drop later ones
       for (unsigned lanes = __ballot_sync(0xffffffffu, cm != 0); lanes;
@@ -209,6 +248,7 @@ __global__ void __launch_bounds__(kDraftThreads, 3) draft_topk_kernel(DraftArgs 
         if (key_value(key) >= thr) insert(key);
         if (cm && !(vmx[i] >= thr)) cm = 0;  // the raised bound excludes the rest of this vector
       }
+    }
     }
     if (cnt == k && thr > published) {  // raise the block's bound (rare once warm)
       if (lane == 0) atomicMax(&s_thr, ordered_u32(thr));
