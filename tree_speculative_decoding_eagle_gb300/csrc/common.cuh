@@ -5,6 +5,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/eagle.h"
 
 namespace eagle {
@@ -214,6 +216,32 @@ template <int K>
 __device__ __forceinline__ void warp_topk(uint64_t (&a)[K]) {
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) list_merge_xor<K>(a, o);
+}
+
+// ---- chained launches (programmatic dependent launch) --------------------
+// The step's kernels are launched so that each may be scheduled while the
+// previous kernel in the stream finishes.  pdl_wait() blocks until that
+// kernel has completed and its writes are visible; every chained kernel calls
+// it before its first global read.  pdl_trigger() lets the next kernel be
+// scheduled; kernels call it once their main work is done.  Both are no-ops
+// for a kernel launched the ordinary way.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_chained(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                  Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // ---- device-side status reporting -----------------------------------------

@@ -114,6 +114,7 @@ __global__ void __launch_bounds__(kDraftThreads, 3) draft_topk_kernel(DraftArgs 
                  ((static_cast<int64_t>(b) * a.D + d) * a.k + j) * a.ld;
   if (tid == 0) s_thr = ordered_u32(-INFINITY);
   if (lane == 0) s_wn[warp] = 0;
+  pdl_wait();
   __syncthreads();  // s_thr and list sizes initialised
   // This CTA's part of the row is a range of 2048-token segments (1024 for
   // fp32); warp w takes segments w, w+8, ...  A segment is held in
@@ -257,6 +258,7 @@ __global__ void __launch_bounds__(kDraftThreads, 3) draft_topk_kernel(DraftArgs 
   }
   if (lane < k) s_wl[warp][lane] = mine;
   if (lane == 0) s_wn[warp] = cnt;
+  pdl_trigger();
 
   // ---- block: softmax statistics and the top k of the warp lists ------------
   {
@@ -380,8 +382,7 @@ size_t draft_workspace_bytes(int B, int D, int k, int V, int vec, int num_sms) {
 
 template <typename T>
 static cudaError_t launch_t(const DraftArgs &a, cudaStream_t st) {
-  draft_topk_kernel<T><<<dim3(a.S, a.B * a.R), kDraftThreads, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_chained(draft_topk_kernel<T>, dim3(a.S, a.B * a.R), dim3(kDraftThreads), 0, st, a);
 }
 
 cudaError_t launch_draft_topk(const void *logits, int dtype, int B, int D, int k, int V,

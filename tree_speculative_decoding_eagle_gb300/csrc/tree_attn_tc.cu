@@ -114,6 +114,7 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
   const int T = np + ntt;  // key tiles of this CTA
   const int producer_warp = MT * 4, mma_warp = MT * 4 + 1;
 
+  pdl_wait();  // inputs of this step (queries, tree K/V, mask) come from earlier kernels
   // ---- Q tiles -> shared memory ---------------------------------------------
   // By TMA when the group size divides 128: a box of (64 columns, G heads,
   // 128/G nodes) lands as 128 rows in (node, grouped head) order, the M-tile
@@ -482,6 +483,7 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
     }
   }
 
+  pdl_trigger();
   // ---- teardown --------------------------------------------------------------
   tc_fence_before();
   __syncthreads();
@@ -675,9 +677,8 @@ static cudaError_t launch_tc_t(const CUtensorMap *maps, const TcArgs &a, const T
     configured = true;
   }
   dim3 grid(p.S, p.mgroups, a.B * a.Hkv);
-  tree_attn_tc_kernel<DH, MT, NK, STAGES><<<grid, Sh::kThreads, Sh::kSmem, st>>>(maps[0], maps[1], maps[2],
-                                                                                maps[3], maps[4], a);
-  return cudaGetLastError();
+  return launch_chained(tree_attn_tc_kernel<DH, MT, NK, STAGES>, grid, dim3(Sh::kThreads), Sh::kSmem, st, maps[0],
+                        maps[1], maps[2], maps[3], maps[4], a);
 }
 
 // Common launcher; block_table == nullptr is the contiguous cache, otherwise

@@ -110,6 +110,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_build_kernel(TreeArgs a) {
   const int32_t *tok = a.tok + static_cast<int64_t>(b) * D * kk;
   const float *conf = a.conf + static_cast<int64_t>(b) * D * kk;
 
+  pdl_wait();
   if (tid == 0) s_bad = 0;
   for (int g = tid; g <= NC; g += blockDim.x) {
     s_row[g] = g == 0 ? 0 : -1;
@@ -269,6 +270,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_build_kernel(TreeArgs a) {
   }
   __syncthreads();
 
+  pdl_trigger();
   // ---- outputs and mask ----------------------------------------------------
   // thread (i, w): node i's fields (w == 0) and mask word w, the latter by
   // walking node i's ancestors in candidate-id space (every ancestor of a
@@ -364,8 +366,7 @@ cudaError_t launch_tree_build(const int32_t *tok, const float *conf, int B, int 
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  tree_build_kernel<<<B, kTreeThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_chained(tree_build_kernel, dim3(B), dim3(kTreeThreads), smem, st, a);
 }
 
 cudaError_t launch_tree_mask(const int32_t *parent, int B, int n, uint64_t *mask, cudaStream_t st) {

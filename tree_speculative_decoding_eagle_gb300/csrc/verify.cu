@@ -50,6 +50,7 @@ __global__ void __launch_bounds__(256) verify_stats_kernel(VerifyArgs a) {
   const int64_t total = static_cast<int64_t>(a.B) * a.n * a.nch;
   const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  pdl_wait();
   for (int64_t task = wid; task < total; task += nwarps) {
     const int64_t row = task / a.nch;
     const int c = static_cast<int>(task % a.nch);
@@ -118,6 +119,7 @@ __global__ void __launch_bounds__(256) verify_stats_kernel(VerifyArgs a) {
     }
     if (lane == 0) a.stats[task] = st;
   }
+  pdl_trigger();
 }
 
 // logit of token t in row `row`, scaled by 1/T
@@ -138,6 +140,7 @@ __global__ void __launch_bounds__(32) verify_walk_kernel(VerifyArgs a) {
   const int n = a.n;
   const int64_t nb = static_cast<int64_t>(b) * n;
   const float sc = a.inv_t * kLog2e;  // logit -> base-2 exponent of exp(x / T), as the statistics pass
+  pdl_wait();
   for (int i = lane; i < n; i += 32) {
     s_par[i] = a.node_parent[nb + i];
     s_tok[i] = a.node_tok[nb + i];
@@ -349,6 +352,7 @@ __global__ void __launch_bounds__(32) verify_walk_kernel(VerifyArgs a) {
     }
     if (bonus < 0) report(a.status, EAGLE_ERR_INVALID);
   }
+  pdl_trigger();
 }
 
 // ---- host side ---------------------------------------------------------------
@@ -366,11 +370,11 @@ static cudaError_t launch_verify_t(const VerifyArgs &a, int num_sms, cudaStream_
   const int64_t cap = static_cast<int64_t>(num_sms) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  if (a.mode == EAGLE_SAMPLE)
-    verify_stats_kernel<T, true><<<static_cast<int>(blocks), 256, 0, st>>>(a);
-  else
-    verify_stats_kernel<T, false><<<static_cast<int>(blocks), 256, 0, st>>>(a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = a.mode == EAGLE_SAMPLE
+                      ? launch_chained(verify_stats_kernel<T, true>, dim3(static_cast<int>(blocks)), dim3(256), 0,
+                                       st, a)
+                      : launch_chained(verify_stats_kernel<T, false>, dim3(static_cast<int>(blocks)), dim3(256), 0,
+                                       st, a);
   if (e != cudaSuccess) return e;
   const size_t smem = sizeof(int) * 4 * static_cast<size_t>(a.n);
   if (smem > 48 * 1024) {
@@ -378,8 +382,7 @@ static cudaError_t launch_verify_t(const VerifyArgs &a, int num_sms, cudaStream_
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  verify_walk_kernel<T><<<a.B, 32, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_chained(verify_walk_kernel<T>, dim3(a.B), dim3(32), smem, st, a);
 }
 
 cudaError_t launch_verify(const void *target, int dtype, int64_t ld, const int32_t *node_tok,
