@@ -530,14 +530,14 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
         const int64_t base = ((static_cast<int64_t>(b) * a.Hq + h) * a.S) * n + i;
         float M = -INFINITY;
 #pragma unroll 8
-        for (int sp = 0; sp < a.S; ++sp) M = fmaxf(M, a.part_ml[(base + static_cast<int64_t>(sp) * n) * 2]);
+        for (int sp = 0; sp < a.S; ++sp) M = fmaxf(M, __ldcg(a.part_ml + (base + static_cast<int64_t>(sp) * n) * 2));
         float Ls = 0.f;
 #pragma unroll 8
         for (int sp = 0; sp < a.S; ++sp) {
           const int64_t pr = base + static_cast<int64_t>(sp) * n;
-          const float ms = a.part_ml[pr * 2];
+          const float ms = __ldcg(a.part_ml + pr * 2);
           const float wgt = (M > -INFINITY && ms > -INFINITY) ? ex2_approx((ms - M) * kLog2e) : 0.f;
-          Ls += wgt * a.part_ml[pr * 2 + 1];
+          Ls += wgt * __ldcg(a.part_ml + pr * 2 + 1);
           s_w[rr * a.S + sp] = wgt;
         }
         const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
@@ -551,14 +551,14 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
         const int rr = item / NV, c = item % NV;
         const int rho = r0 + rr, i = rho / a.G, h = g * a.G + rho % a.G;
         const int64_t base = ((static_cast<int64_t>(b) * a.Hq + h) * a.S) * n + i;
+        // every split's partial is loaded (an empty split holds zeros and
+        // weight 0), so the loads of one item are all in flight together
         float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
+#pragma unroll 8
         for (int sp = 0; sp < a.S; ++sp) {
           const float wgt = s_w[rr * a.S + sp];
-          if (wgt != 0.f) {
-            const float4 po = reinterpret_cast<const float4 *>(a.part_o + (base + static_cast<int64_t>(sp) * n) * DH)[c];
-            o.x += wgt * po.x; o.y += wgt * po.y; o.z += wgt * po.z; o.w += wgt * po.w;
-          }
+          const float4 po = __ldcg(reinterpret_cast<const float4 *>(a.part_o + (base + static_cast<int64_t>(sp) * n) * DH) + c);
+          o.x = fmaf(wgt, po.x, o.x); o.y = fmaf(wgt, po.y, o.y); o.z = fmaf(wgt, po.z, o.z); o.w = fmaf(wgt, po.w, o.w);
         }
         const int64_t orow = (static_cast<int64_t>(b) * n + i) * a.Hq + h;
         __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y);
