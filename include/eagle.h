@@ -259,6 +259,9 @@ int eagle_tree_mask(const int32_t *node_parent, int B, int n, uint64_t *mask,
  * probabilities rounded to bf16 for the P.V product); fp32 inputs run on the
  * CUDA cores.  Cache rows at or beyond kv_len[b] are never read; every row
  * of k_tree / v_tree must hold finite values.
+ * Workspace: none for bf16 (the KV splits of a head merge through the
+ * distributed shared memory of one thread-block cluster, so the size is 0);
+ * fp32 partial results and weights for fp32.
  * Limits: Hq % Hkv == 0, dh in {64, 128}, 1 <= n <= 4096, B*Hkv <= 65535.
  * ------------------------------------------------------------------------ */
 size_t eagle_tree_attn_workspace_size(int dtype, int B, int n, int Hq, int Hkv,

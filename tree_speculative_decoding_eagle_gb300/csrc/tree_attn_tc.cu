@@ -27,6 +27,10 @@
 //     mbarriers), so one M-tile's exponents overlap the other's MMAs and max
 //     pass instead of both competing for the same issue slots.
 // Tensor memory per M-tile: S (NK columns), P (NK/2), O (dh).
+// KV split (few heads: S <= 8 CTAs share one (b, g, M-group)): the S CTAs
+// are one thread-block cluster; each leaves its unnormalised O and (m, l)
+// in its own shared memory and merges 1/S of the rows from all S through
+// distributed shared memory, so partial results never reach HBM.
 // Every wait is bounded; a timeout raises EAGLE_ERR_TIMEOUT in the status
 // word and the CTA drains its copies and MMAs, frees tensor memory and exits.
 #include <mutex>
@@ -52,8 +56,6 @@ struct TcArgs {
   float scale_log2;  // softmax scale times log2(e)
   __nv_bfloat16 *out;
   float *lse;
-  float *part_o, *part_ml;
-  uint32_t *tickets;  // split merge: one counter per (b, g, M-group), reset by the last CTA
   int q_tma;          // 1: Q tiles arrive by TMA (128 % G == 0), else plain loads
   int32_t *status;
 };
@@ -65,7 +67,7 @@ struct TcShape {
   static constexpr int kTileBytes = kRegions * NK * 128;     // one K (or V) tile
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kBarOff = kQBytes + STAGES * kStageBytes;
-  static constexpr int kNumBars = 2 * STAGES + 4 * MT + 4;
+  static constexpr int kNumBars = 2 * STAGES + 4 * MT + 6;
   static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;  // + alignment slack
   static constexpr int kThreads = MT * 128 + 64;
   static constexpr int kColS = 0;                            // S_t at t*NK
@@ -74,7 +76,13 @@ struct TcShape {
   static constexpr int kCols = kColO + MT * DH;
   static constexpr int kTmemCols = kCols <= 128 ? 128 : (kCols <= 256 ? 256 : 512);
   static_assert(kCols <= 512, "tensor memory budget");
+  // split merge: fp32 O rows in the stage buffers, (m, l) in Q's
+  static_assert(MT * 128 * DH * 4 <= STAGES * kStageBytes, "partial O fits the stage buffers");
+  static_assert(MT * 128 * 8 <= kQBytes, "(m, l) fit the Q buffer");
 };
+
+// Most KV splits of one (sequence, KV head, M-group): one cluster of CTAs.
+constexpr int kMaxClusterSplits = 8;
 
 template <int DH, int MT, int NK, int STAGES>
 __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
@@ -98,6 +106,8 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
   uint64_t *teardown = o_done + MT;
   uint64_t *turn = teardown + 1;  // exponent-pass token of M-tile 0 / 1
   uint64_t *q_full = turn + 2;    // the Q tiles (TMA)
+  uint64_t *cl_full = q_full + 1; // split merge: every CTA of the cluster has its partials in shared memory
+  uint64_t *cl_done = cl_full + 1;  // split merge: every CTA of the cluster has read its peers
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Sh::kNumBars);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -151,6 +161,8 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
     mbar_init(&turn[0], 4);
     mbar_init(&turn[1], 4);
     mbar_init(q_full, 1);
+    mbar_init(cl_full, a.S);
+    mbar_init(cl_done, a.S);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -161,14 +173,18 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (a.S > 1) cluster_arrive_relaxed();  // waited on before the first signal to a peer
   const uint32_t tmem = *tmem_slot;
 
   int issued = 0;  // producer: tiles issued
+  // softmax threads with S > 1: this row's final (m, l), kept for the merge
+  bool part_have = false;
+  float part_m = -INFINITY, part_l = 0.f;
 
   if (warp == producer_warp) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
-      if (a.q_tma) {
+      if (a.q_tma && T > 0) {
         mbar_arrive_expect_tx(q_full, MT * Sh::kRegions * 16384);
         for (int t = 0; t < MT; ++t)
 #pragma unroll
@@ -443,43 +459,37 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
     }
     if (ok && T > 0 && !warp_wait(&o_done[t], (T - 1) & 1, abort_flag)) ok = false;
     tc_fence_after();
-    // tcgen05.ld is warp-collective (.sync.aligned): every lane executes it,
-    // rows past the last node only skip the global writes
-    const int h = g * a.G + hh;
-    const int64_t orow = (static_cast<int64_t>(b) * n + i) * a.Hq + h;
-    const int64_t prow_ = ((static_cast<int64_t>(b) * a.Hq + h) * a.S + split) * n + i;
     const bool have = ok && T > 0;
-    const float inv = (have && l > 0.f) ? 1.f / l : 0.f;
+    if (a.S > 1) {
+      // split: (m, l) wait for the cluster merge; O stays in tensor memory
+      // until every MMA of the CTA is done (the teardown barrier)
+      part_have = have;
+      part_m = m;
+      part_l = l;
+    } else {
+      // tcgen05.ld is warp-collective (.sync.aligned): every lane executes
+      // it, rows past the last node only skip the global writes
+      const int h = g * a.G + hh;
+      const int64_t orow = (static_cast<int64_t>(b) * n + i) * a.Hq + h;
+      const float inv = (have && l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll
-    for (int c0 = 0; c0 < DH; c0 += 32) {
-      float o[32];
-      if (have) {
-        tmem_ld32(tO + c0, o);
-      } else {
+      for (int c0 = 0; c0 < DH; c0 += 32) {
+        float o[32];
+        if (have) {
+          tmem_ld32(tO + c0, o);
+        } else {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) o[c] = 0.f;
-      }
-      if (!row_ok) continue;
-      if (a.S == 1) {
+          for (int c = 0; c < 32; ++c) o[c] = 0.f;
+        }
+        if (!row_ok) continue;
         __nv_bfloat162 hv[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) hv[e] = __floats2bfloat162_rn(o[2 * e] * inv, o[2 * e + 1] * inv);
         uint4 *dst = reinterpret_cast<uint4 *>(a.out + orow * DH + c0);
 #pragma unroll
         for (int e = 0; e < 4; ++e) dst[e] = reinterpret_cast<const uint4 *>(hv)[e];
-      } else {
-        float4 *dst = reinterpret_cast<float4 *>(a.part_o + prow_ * DH + c0);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) dst[e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
       }
-    }
-    if (row_ok) {
-      if (a.S == 1) {
-        if (a.lse) a.lse[orow] = have ? (m + __log2f(l)) * kLn2 : -INFINITY;
-      } else {
-        a.part_ml[prow_ * 2 + 0] = have ? m * kLn2 : -INFINITY;
-        a.part_ml[prow_ * 2 + 1] = have ? l : 0.f;
-      }
+      if (row_ok && a.lse) a.lse[orow] = have ? (m + __log2f(l)) * kLn2 : -INFINITY;
     }
   }
 
@@ -498,77 +508,130 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
     }
     if (warp == producer_warp && lane == 0) {
       // copies still in flight complete before shared memory is released
-      if (a.q_tma) mbar_wait(q_full, 0, &never, 100000000ull);
+      if (a.q_tma && T > 0) mbar_wait(q_full, 0, &never, 100000000ull);
       for (int j = max(0, issued - STAGES); j < issued; ++j)
         mbar_wait(&kv_full[j % STAGES], (j / STAGES) & 1, &never, 100000000ull);
     }
     __syncthreads();
   }
+  if (a.S > 1 && warp < MT * 4) {
+    // this CTA's unnormalised O rows (fp32) into the stage buffers and its
+    // (m, l) pairs into the Q buffer: every MMA and copy has completed.  Row
+    // r's 16-byte chunk c sits at chunk c ^ (r & 7) of the row, so the 32
+    // rows of a warp store to distinct banks.
+    const int t = warp >> 2, qtr = warp & 3, rl = t * 128 + qtr * 32 + lane;
+    const uint32_t tO = tmem + (static_cast<uint32_t>(qtr * 32) << 16) + Sh::kColO + t * DH;
+    const bool have = part_have && !*abort_flag;
+    float4 *prow = reinterpret_cast<float4 *>(sKV) + rl * (DH / 4);
+#pragma unroll
+    for (int c0 = 0; c0 < DH; c0 += 32) {
+      float o[32];
+      if (__all_sync(0xffffffffu, have)) {
+        tmem_ld32(tO + c0, o);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) o[c] = 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        prow[(c0 / 4 + e) ^ (rl & 7)] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+    }
+    reinterpret_cast<float2 *>(sQ)[rl] = have ? make_float2(part_m * kLn2, part_l) : make_float2(-INFINITY, 0.f);
+    fence_acq_rel_cluster();
+  }
+  tc_fence_before();
+  __syncthreads();
   if (warp == mma_warp) tmem_dealloc(tmem, Sh::kTmemCols);
 
-  // ---- split merge: the last CTA of this (b, g, M-group) combines the S
-  // partial results (max m, sum l, unnormalised O) of its rows ------------
+  // ---- split merge across the cluster ----------------------------------------
+  // The S splits of this (b, g, M-group) are one cluster.  Each CTA signals
+  // every peer that its partials are in shared memory, then merges rows
+  // [rank*per, (rank+1)*per) of the group by reading all S partials through
+  // distributed shared memory: out = sum_s w_s O_s with w_s = exp(m_s - M) / L,
+  // M = max_s m_s, L = sum_s exp(m_s - M) l_s.  A second round of signals
+  // keeps every CTA's shared memory alive until its peers have read it.
+  // Both waits are bounded; a timeout raises EAGLE_ERR_TIMEOUT.
   if (a.S > 1) {
-    __shared__ int s_is_last;
-    __threadfence();  // this CTA's partials are visible before its ticket
-    __syncthreads();
+    cluster_wait();  // every peer has initialised its barriers
+    const uint32_t rank = cluster_ctarank();
+    if (tid < a.S) mbar_arrive_remote(mapa_shared(smem_u32(cl_full), tid));  // one peer per thread
+    // one thread polls; the CTA barrier releases the others
     if (tid == 0) {
-      const int idx = bg * gridDim.y + mg;
-      const uint32_t old = atomicAdd(&a.tickets[idx], 1u);
-      s_is_last = old == static_cast<uint32_t>(a.S - 1);
-      if (s_is_last) a.tickets[idx] = 0;  // every split has arrived: ready for the next call
+      *abort_flag = mbar_wait_cluster(cl_full, 0, 200000000ull) ? 0 : 1;
+      if (*abort_flag) report(a.status, EAGLE_ERR_TIMEOUT);
     }
     __syncthreads();
-    if (s_is_last) {
-      __threadfence();
-      // (1) per row: the splits' weights exp(m_s - M) / L into shared memory
-      // (the stage buffers, all copies done), and the row's lse
-      const int r0 = mg * MT * 128, nr = max(0, min(rows_total, r0 + MT * 128) - r0);
-      float *s_w = reinterpret_cast<float *>(sKV);  // [nr][S]
-      for (int rr = tid; rr < nr; rr += Sh::kThreads) {
-        const int rho = r0 + rr, i = rho / a.G, h = g * a.G + rho % a.G;
-        const int64_t base = ((static_cast<int64_t>(b) * a.Hq + h) * a.S) * n + i;
+    const bool cok = *abort_flag == 0;
+    const int r0 = mg * MT * 128, nr = max(0, min(rows_total, r0 + MT * 128) - r0);
+    const int per = (nr + a.S - 1) / a.S;
+    const int q0 = min(nr, static_cast<int>(rank) * per), q1 = min(nr, q0 + per);
+    uint32_t r_o[kMaxClusterSplits];  // the peers' O buffers
+#pragma unroll
+    for (int sp = 0; sp < kMaxClusterSplits; ++sp) r_o[sp] = mapa_shared(smem_u32(sKV), sp < a.S ? sp : 0);
+    // four output columns per item, two items per thread at a time.  The NV
+    // items of a row sit in NV consecutive lanes: lane c of the row loads
+    // split c's (m, l) and the row's lanes share them by shuffles; every
+    // item loads its S partial chunks, all in flight together.
+    constexpr int NV = DH / 4;
+    static_assert(NV == 16 || NV == 32, "a row's items fill half or all of a warp");
+    constexpr int kItems = 2;
+    const int n_items = (q1 - q0) * NV;  // a multiple of NV: a row's lanes agree on validity
+    const uint32_t ml_local = smem_u32(sQ);
+    for (int base = tid; cok && base - lane < n_items; base += kItems * Sh::kThreads) {
+      float2 mine[kItems];
+      float4 po[kItems][kMaxClusterSplits];
+#pragma unroll
+      for (int u = 0; u < kItems; ++u) {
+        const int item = base + u * Sh::kThreads;
+        const int rr = q0 + item / NV, c = item % NV;
+        const bool valid = item < n_items;
+        mine[u] = (valid && c < a.S) ? ld_cluster_f2(mapa_shared(ml_local, c) + rr * 8) : make_float2(-INFINITY, 0.f);
+        const uint32_t off = static_cast<uint32_t>((rr * NV + (c ^ (rr & 7))) * 16);
+#pragma unroll
+        for (int sp = 0; sp < kMaxClusterSplits; ++sp)
+          po[u][sp] = (valid && sp < a.S) ? ld_cluster_f4(r_o[sp] + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kItems; ++u) {
+        const int item = base + u * Sh::kThreads;
+        float2 ml[kMaxClusterSplits];
+#pragma unroll
+        for (int sp = 0; sp < kMaxClusterSplits; ++sp) {
+          ml[sp].x = __shfl_sync(0xffffffffu, mine[u].x, sp, NV);
+          ml[sp].y = __shfl_sync(0xffffffffu, mine[u].y, sp, NV);
+          if (sp >= a.S) ml[sp] = make_float2(-INFINITY, 0.f);
+        }
+        if (item >= n_items) continue;
+        const int rr = q0 + item / NV, c = item % NV;
         float M = -INFINITY;
-#pragma unroll 8
-        for (int sp = 0; sp < a.S; ++sp) M = fmaxf(M, __ldcg(a.part_ml + (base + static_cast<int64_t>(sp) * n) * 2));
+#pragma unroll
+        for (int sp = 0; sp < kMaxClusterSplits; ++sp) M = fmaxf(M, ml[sp].x);
         float Ls = 0.f;
-#pragma unroll 8
-        for (int sp = 0; sp < a.S; ++sp) {
-          const int64_t pr = base + static_cast<int64_t>(sp) * n;
-          const float ms = __ldcg(a.part_ml + pr * 2);
-          const float wgt = (M > -INFINITY && ms > -INFINITY) ? ex2_approx((ms - M) * kLog2e) : 0.f;
-          Ls += wgt * __ldcg(a.part_ml + pr * 2 + 1);
-          s_w[rr * a.S + sp] = wgt;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int sp = 0; sp < kMaxClusterSplits; ++sp) {
+          const float x = ml[sp].x;
+          const float wgt = (M > -INFINITY && x > -INFINITY) ? ex2_approx((x - M) * kLog2e) : 0.f;
+          Ls = fmaf(wgt, ml[sp].y, Ls);
+          o.x = fmaf(wgt, po[u][sp].x, o.x); o.y = fmaf(wgt, po[u][sp].y, o.y);
+          o.z = fmaf(wgt, po[u][sp].z, o.z); o.w = fmaf(wgt, po[u][sp].w, o.w);
         }
         const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-        for (int sp = 0; sp < a.S; ++sp) s_w[rr * a.S + sp] *= inv;
-        if (a.lse) a.lse[(static_cast<int64_t>(b) * n + i) * a.Hq + h] = Ls > 0.f ? M + __logf(Ls) : -INFINITY;
-      }
-      __syncthreads();
-      // (2) out = sum_s w_s O_s, four columns per item
-      constexpr int NV = DH / 4;
-      for (int item = tid; item < nr * NV; item += Sh::kThreads) {
-        const int rr = item / NV, c = item % NV;
         const int rho = r0 + rr, i = rho / a.G, h = g * a.G + rho % a.G;
-        const int64_t base = ((static_cast<int64_t>(b) * a.Hq + h) * a.S) * n + i;
-        // every split's partial is loaded (an empty split holds zeros and
-        // weight 0), so the loads of one item are all in flight together
-        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-        for (int sp = 0; sp < a.S; ++sp) {
-          const float wgt = s_w[rr * a.S + sp];
-          const float4 po = __ldcg(reinterpret_cast<const float4 *>(a.part_o + (base + static_cast<int64_t>(sp) * n) * DH) + c);
-          o.x = fmaf(wgt, po.x, o.x); o.y = fmaf(wgt, po.y, o.y); o.z = fmaf(wgt, po.z, o.z); o.w = fmaf(wgt, po.w, o.w);
-        }
         const int64_t orow = (static_cast<int64_t>(b) * n + i) * a.Hq + h;
-        __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y);
-        __nv_bfloat162 hi = __floats2bfloat162_rn(o.z, o.w);
+        __nv_bfloat162 lo = __floats2bfloat162_rn(o.x * inv, o.y * inv);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(o.z * inv, o.w * inv);
         uint2 packed;
         packed.x = *reinterpret_cast<const uint32_t *>(&lo);
         packed.y = *reinterpret_cast<const uint32_t *>(&hi);
         reinterpret_cast<uint2 *>(a.out + orow * DH)[c] = packed;
+        if (c == 0 && a.lse) a.lse[orow] = Ls > 0.f ? M + __logf(Ls) : -INFINITY;
       }
     }
+    __syncthreads();  // this CTA is done reading its peers
+    if (tid < a.S) mbar_arrive_remote(mapa_shared(smem_u32(cl_done), tid));
+    // stay (and keep this CTA's shared memory) until every peer is done
+    if (tid == 0 && !mbar_wait_cluster(cl_done, 0, 200000000ull)) report(a.status, EAGLE_ERR_TIMEOUT);
   }
 }
 
@@ -625,8 +688,8 @@ struct TcPlan {
 };
 
 // Launch plan: M-tiles per CTA, key-tile width, and the KV split S chosen to
-// minimise (waves of CTAs) x (key tiles per CTA + the extra traffic a split's
-// partial results cost, in key-tile units).
+// minimise (waves of CTAs) x (key tiles per CTA + the cost of merging a
+// split's partial results, in key-tile units).
 static TcPlan tc_plan(int B, int n, int Hq, int Hkv, int dh, int Lmax, int num_sms) {
   TcPlan p;
   const int G = Hq / Hkv;
@@ -641,7 +704,7 @@ static TcPlan tc_plan(int B, int n, int Hq, int Hkv, int dh, int Lmax, int num_s
   const double split_cost = static_cast<double>(G) * n * 64.0 / p.NK / 32.0 / p.mgroups;
   int best = 1;
   double best_cost = 1e30;
-  for (int S = 1; S <= 32 && S <= ptiles; ++S) {
+  for (int S = 1; S <= kMaxClusterSplits && S <= ptiles; ++S) {
     const int64_t waves = (base * S + slots - 1) / slots;
     const double per_cta = static_cast<double>((ptiles + S - 1) / S) + (S > 1 ? split_cost : 0.0);
     const double cost = waves * per_cta;
@@ -654,14 +717,8 @@ static TcPlan tc_plan(int B, int n, int Hq, int Hkv, int dh, int Lmax, int num_s
   return p;
 }
 
-// Split workspace: fp32 partial O [B, Hq, S, n, dh], (m, l) [B, Hq, S, n, 2],
-// then one merge ticket per (b, g, M-group).
-size_t attn_tc_workspace_bytes(int B, int n, int Hq, int Hkv, int dh, int Lmax, int num_sms) {
-  const TcPlan p = tc_plan(B, n, Hq, Hkv, dh, Lmax, num_sms);
-  if (p.S == 1) return 0;
-  return sizeof(float) * static_cast<size_t>(B) * Hq * p.S * n * (dh + 2) +
-         sizeof(uint32_t) * static_cast<size_t>(B) * Hkv * p.mgroups;
-}
+// The splits merge through distributed shared memory: no workspace.
+size_t attn_tc_workspace_bytes(int, int, int, int, int, int, int) { return 0; }
 
 template <int DH, int MT, int NK, int STAGES>
 static cudaError_t launch_tc_t(const CUtensorMap *maps, const TcArgs &a, const TcPlan &p, cudaStream_t st) {
@@ -676,9 +733,10 @@ static cudaError_t launch_tc_t(const CUtensorMap *maps, const TcArgs &a, const T
     if (e != cudaSuccess) return e;
     configured = true;
   }
+  // the S splits of one (b, g, M-group) form one cluster
   dim3 grid(p.S, p.mgroups, a.B * a.Hkv);
-  return launch_chained(tree_attn_tc_kernel<DH, MT, NK, STAGES>, grid, dim3(Sh::kThreads), Sh::kSmem, st, maps[0],
-                        maps[1], maps[2], maps[3], maps[4], a);
+  return launch_chained_cluster(tree_attn_tc_kernel<DH, MT, NK, STAGES>, grid, dim3(Sh::kThreads), Sh::kSmem, st,
+                                p.S, maps[0], maps[1], maps[2], maps[3], maps[4], a);
 }
 
 // Common launcher; block_table == nullptr is the contiguous cache, otherwise
@@ -714,9 +772,6 @@ static cudaError_t launch_tc_common(const void *q, const void *k_cache, const vo
   a.scale_log2 = scale * kLog2e;
   a.out = reinterpret_cast<__nv_bfloat16 *>(out);
   a.lse = lse;
-  a.part_o = reinterpret_cast<float *>(ws);
-  a.part_ml = a.part_o + static_cast<size_t>(B) * Hq * p.S * n * dh;
-  a.tickets = reinterpret_cast<uint32_t *>(a.part_ml + static_cast<size_t>(B) * Hq * p.S * n * 2);
   a.q_tma = q_tma ? 1 : 0;
   a.status = status;
   cudaError_t e;
