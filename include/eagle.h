@@ -88,9 +88,11 @@ int eagle_version(void);
  *   tok     device int32 [B, D, k, k]     (out)
  *   conf    device float [B, D, k, k]     (out)
  *   stats   device float [B, D, k, 2]     (out; may be NULL)
- *   status  device int32 (out; may be NULL): EAGLE_ERR_TIMEOUT if a bounded
- *           wait on the kernel's own copies gave up (the row is then not
+ *   status  device int32 (out; may be NULL): EAGLE_ERR_TIMEOUT if the
+ *           bounded wait of a row's merge gave up (the row is then not
  *           written)
+ * Workspace: none (the size is 0); a row split over several CTAs merges
+ * through the shared memory of their thread-block cluster.
  * Limits: 1 <= k <= 32, k <= V, D >= 1, B >= 1.
  * ------------------------------------------------------------------------ */
 size_t eagle_draft_topk_workspace_size(int B, int D, int k, int V);
@@ -107,18 +109,9 @@ int eagle_draft_topk(const void *logits, int dtype, int B, int D, int k, int V,
  * of a host runtime that hands over only input and output buffers and owns
  * all device memory, or processes whose device-memory budget is fixed up
  * front.  Same arguments and results as eagle_draft_topk, without the
- * workspace.  It allocates nothing: its scratch is a fixed array of
- * EAGLE_NOALLOC_SCRATCH_BYTES compiled into the library, present on every GPU
- * that loads the library until the process exits.  The array's device
- * address is looked up on the first call made while a device is current.
- * Sizes whose scratch would exceed the array return EAGLE_ERR_WORKSPACE
- * (eagle_draft_topk_workspace_size gives the need).  Every call on a device
- * shares the one array, so calls that may overlap on the GPU (different
- * streams or host threads) race and must be serialised by the caller; each
- * call clears the part of the array that must start at zero.
+ * workspace arguments (the stage needs none).  It allocates nothing; calls
+ * on different streams may overlap.
  * ------------------------------------------------------------------------ */
-#define EAGLE_NOALLOC_SCRATCH_BYTES (1u << 17) /* 128 KiB */
-
 int eagle_draft_topk_noalloc(const void *logits, int dtype, int B, int D, int k,
                              int V, int64_t ld, int32_t *tok, float *conf,
                              float *stats, int32_t *status,

@@ -98,5 +98,6 @@ def test_invalid_arguments_are_rejected_on_the_host(lib):
 
 def test_workspace_queries_are_host_only(lib):
     assert lib.eagle_verify_workspace_size(8, 50, 32000) == 16 * 8 * 51 * 16
-    assert lib.eagle_draft_topk_workspace_size(1, 6, 10, 32000) > 0
+    assert lib.eagle_draft_topk_workspace_size(1, 6, 10, 32000) == 0   # parts merge in cluster shared memory
+    assert lib.eagle_draft_topk_workspace_size(64, 6, 10, 201088) == 0
     assert lib.eagle_draft_topk_workspace_size(0, 6, 10, 32000) == 0

@@ -1,0 +1,79 @@
+"""GPU parity of the draft softmax / top-k stage on rows that stress the
+selection: every token tied (a constant row), thousands tied at the top (a
+two-level row), exactly k finite values (the rest -inf), a row quantised to
+a handful of levels, and ordinary rows.  Tokens must equal the oracle's
+(ties -> lower token id), confidences and log-sums within the parity
+tolerances.
+
+Shapes cover both launch forms: one sequence of Llama-2-7B-shaped rows
+(few rows: 16-warp CTAs, each row split over a cluster of CTAs) and four
+sequences (8-warp CTAs), in bf16 and fp32, plus k = 32.
+"""
+import numpy as np
+import pytest
+import torch
+
+import tree_speculative_decoding_eagle_gb300 as eg
+from oracle import draft as odraft
+
+from paritylib import CONF_RTOL, LOGZ_TOL
+
+pytestmark = pytest.mark.gpu
+
+
+def edge_rows(B, D, k, V, seed):
+    """[B, D, k, V] float32 logits, each used row drawn from one of the kinds."""
+    rng = np.random.default_rng(seed)
+    x = np.empty((B, D, k, V), dtype=np.float32)
+    kinds = ["constant", "two-level", "k-finite", "levels", "normal"]
+    for b in range(B):
+        for i, (d, j) in enumerate(odraft.used_rows(D, k)):
+            kind = kinds[(i + b) % len(kinds)]
+            if kind == "constant":
+                row = np.full(V, -3.0, dtype=np.float32)
+            elif kind == "two-level":
+                row = np.where(rng.random(V) < 0.5, 1.0, 0.0).astype(np.float32)
+            elif kind == "k-finite":
+                row = np.full(V, -np.inf, dtype=np.float32)
+                pos = rng.choice(V, size=k, replace=False)
+                row[pos] = rng.normal(size=k).astype(np.float32)
+            elif kind == "levels":
+                row = np.floor(rng.normal(size=V) * 2.0).astype(np.float32)
+            else:
+                row = (4.0 * rng.normal(size=V)).astype(np.float32)
+            x[b, d, j] = row
+        for j in range(1, k):          # rows never read by the stage
+            x[b, 0, j] = 0.0
+    return x
+
+
+CASES = [
+    ("bf16", 1, 6, 10, 32000),
+    ("bf16", 4, 6, 10, 32000),
+    ("f32", 1, 6, 10, 32000),
+    ("f32", 4, 6, 10, 32000),
+    ("bf16", 1, 3, 32, 4096),
+    ("bf16", 2, 2, 4, 201088),
+]
+
+
+@pytest.mark.parametrize("dtype,B,D,k,V", CASES)
+def test_draft_edge_rows(dtype, B, D, k, V):
+    x = edge_rows(B, D, k, V, seed=B * 1000 + V + k)
+    td = torch.bfloat16 if dtype == "bf16" else torch.float32
+    logits = torch.from_numpy(x).to(td)
+    exact = logits.float().numpy()          # the values the kernel sees
+    tok_o, conf_o, stats_o = odraft.draft_topk(exact, k)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(2):                       # twice: nothing carries over between calls
+        tok, conf, stats = eg.draft_topk(logits.cuda(), k, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        tok, conf, stats = tok.cpu().numpy(), conf.cpu().numpy(), stats.cpu().numpy()
+        for b in range(B):
+            for d, j in odraft.used_rows(D, k):
+                assert (tok[b, d, j] == tok_o[b, d, j]).all(), (b, d, j)
+                np.testing.assert_allclose(conf[b, d, j], conf_o[b, d, j], rtol=CONF_RTOL, atol=1e-30)
+                assert stats[b, d, j, 0] == np.float32(stats_o[b, d, j, 0])
+                lz = stats_o[b, d, j, 1]
+                assert abs(stats[b, d, j, 1] - lz) <= LOGZ_TOL * max(1.0, abs(lz))

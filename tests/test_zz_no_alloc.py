@@ -1,8 +1,8 @@
 """eagle_draft_topk_noalloc: the draft stage for callers that cannot give the
 library scratch memory (runtimes that hand over only input and output
 buffers, or fixed device-memory budgets).  It must produce what
-eagle_draft_topk produces, call after call, using only its built-in scratch
-array.  This file is named to be collected last."""
+eagle_draft_topk produces, call after call, with no scratch at all.  This
+file is named to be collected last."""
 import ctypes
 
 import numpy as np
@@ -25,14 +25,12 @@ def call_noalloc(lib, logits, k, tok, conf, stats, status):
                                         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
-def test_oversized_request_is_refused_on_the_host():
+def test_invalid_request_is_refused_on_the_host():
     lib = eg.load_library()
-    fake = ctypes.c_void_p(0x1000)   # never dereferenced: the size check comes first
-    # 1000 sequences x 51 rows need 204 KB of merge tickets, above the 128 KiB array
-    need = lib.eagle_draft_topk_workspace_size(1000, 6, 10, 32000)
-    assert need > (1 << 17)
-    rc = lib.eagle_draft_topk_noalloc(fake, eg.BF16, 1000, 6, 10, 32000, 32000, fake, fake, None, None, None)
-    assert rc == -4
+    fake = ctypes.c_void_p(0x1000)   # never dereferenced: the argument checks come first
+    assert lib.eagle_draft_topk_noalloc(fake, eg.BF16, 1, 6, 0, 32000, 32000, fake, fake, None, None, None) == -1
+    assert lib.eagle_draft_topk_noalloc(fake, eg.BF16, 1, 6, 10, 32000, 31999, fake, fake, None, None, None) == -1
+    assert lib.eagle_draft_topk_noalloc(None, eg.BF16, 1, 6, 10, 32000, 32000, fake, fake, None, None, None) == -1
 
 
 @pytest.mark.gpu

@@ -5,8 +5,11 @@
 // used row: M = max, Z = sum exp(x - M), the k largest logits (ties -> lower
 // token id) and c = exp(x - M) / Z.
 //
-// One pass over HBM.  A row is split into parts of 8 warps x 2048 tokens
-// (bf16; 1024 for fp32), one CTA per part.  Each warp holds a segment in
+// One pass over HBM.  A row is split into S <= 8 parts, one CTA each; the
+// parts of a row form one thread-block cluster.  Few rows (each part fits
+// one segment per warp with the parts of all rows resident at once) take
+// 16-warp CTAs with 1024-token segments; many rows take 8-warp CTAs with
+// 2048-token segments, three per SM.  Each warp holds a segment in
 // registers (all 16-byte loads in flight at once) and visits it twice: lane
 // maxima, then the sum of exp(x - segment max), folded into a running
 // (max, sum).  Top-k selection works on unique 64-bit keys (logit order,
@@ -16,35 +19,58 @@
 // k-th key bounds the part from below, so values under the bound (shared
 // block-wide as a maximum over the warps) are never looked at; before the
 // list is full, the k-th largest lane maximum is the bound.  The warp lists
-// merge block-wide by rank counting in shared memory.  With S > 1 the last
-// CTA of a row to finish (atomic ticket in the workspace) merges the S
-// partial results; no CTA ever waits for another.
+// merge block-wide: only keys at or above the block's bound are kept, and
+// their ranks are counted.  With S > 1 every part pushes its k keys and
+// (max, sum) into the shared memory of the row's first CTA and signals its
+// mbarrier; that CTA merges them (a bounded wait; a timeout raises
+// EAGLE_ERR_TIMEOUT and leaves the row unwritten).
 #include "common.cuh"
+#include "sm100.cuh"
 
 namespace eagle {
 
+using sm100::cluster_arrive_relaxed;
+using sm100::cluster_ctarank;
+using sm100::cluster_wait;
+using sm100::mapa_shared;
+using sm100::mbar_init;
+using sm100::mbar_init_fence;
+using sm100::mbar_wait_cluster;
+using sm100::smem_u32;
+
 struct DraftArgs {
   const void *logits;
-  int B, D, k, V, R, S;  // R = used rows per sequence, S = splits per row
+  int B, D, k, V, R, S;  // R = used rows per sequence, S = parts per row (one cluster)
   int64_t ld;
   int32_t *tok;
   float *conf;
   float *stats;
-  unsigned char *ws;     // [counters (B*R u32, 256-aligned)][records]
   int32_t *status;
 };
 
-constexpr int kDraftThreads = 256;
-constexpr int kBatchCap = 128;  // candidates of one segment merged as a batch (the warp's buffer)
-constexpr int kDraftVecPerLane = 8;  // 16-byte vectors each lane holds in registers
+constexpr int kBatchCap = 128;    // candidates of one segment merged as a batch (the warp's buffer)
+constexpr int kMaxDraftParts = 8;  // parts of one row: one cluster
 
-// Workspace: [tickets: u32 per row][(max, sum) per row and split][k keys per
-// row and split], each part 256-byte aligned.
-__host__ __device__ inline size_t draft_counter_bytes(int B, int R) {
-  return (static_cast<size_t>(B) * R * sizeof(uint32_t) + 255) / 256 * 256;
+// Number of keys of set[0..n) greater than `key` (set 16-byte aligned).
+// Every lane of a warp reads the same addresses (broadcast), four 16-byte
+// loads in flight.  Zero keys (empty slots) are never greater.
+__device__ __forceinline__ int count_greater(uint64_t key, const uint64_t *set, int n) {
+  const ulonglong2 *s2 = reinterpret_cast<const ulonglong2 *>(set);
+  int r = 0;
+#pragma unroll 4
+  for (int q = 0; q < n / 2; ++q) {
+    const ulonglong2 v = s2[q];
+    r += (v.x > key) + (v.y > key);
+  }
+  if (n & 1) r += set[n - 1] > key;
+  return r;
 }
-__host__ __device__ inline size_t draft_ms_bytes(int B, int R, int S) {
-  return (static_cast<size_t>(B) * R * S * sizeof(float2) + 255) / 256 * 256;
+
+__device__ __forceinline__ uint64_t shfl_up_u64(uint64_t v, int d) {
+  uint32_t lo = static_cast<uint32_t>(v), hi = static_cast<uint32_t>(v >> 32);
+  lo = __shfl_up_sync(0xffffffffu, lo, d);
+  hi = __shfl_up_sync(0xffffffffu, hi, d);
+  return (static_cast<uint64_t>(hi) << 32) | lo;
 }
 
 // Bitonic sort of one float per lane across the warp, descending by lane.
@@ -62,20 +88,6 @@ __device__ __forceinline__ float warp_sort_desc(float x, int lane) {
   return x;
 }
 
-// Rank of `key` among set[0..n): the number of larger keys (keys are unique).
-__device__ __forceinline__ int rank_in(uint64_t key, const uint64_t *set, int n) {
-  int r = 0;
-  for (int q = 0; q < n; ++q) r += set[q] > key;
-  return r;
-}
-
-__device__ __forceinline__ uint64_t shfl_up_u64(uint64_t v, int d) {
-  uint32_t lo = static_cast<uint32_t>(v), hi = static_cast<uint32_t>(v >> 32);
-  lo = __shfl_up_sync(0xffffffffu, lo, d);
-  hi = __shfl_up_sync(0xffffffffu, hi, d);
-  return (static_cast<uint64_t>(hi) << 32) | lo;
-}
-
 // Element e of a 16-byte vector as float (no indexed register access).
 template <typename T> __device__ __forceinline__ float elem_of(const uint4 &v, int e);
 template <> __device__ __forceinline__ float elem_of<__nv_bfloat16>(const uint4 &v, int e) {
@@ -87,42 +99,70 @@ template <> __device__ __forceinline__ float elem_of<float>(const uint4 &v, int 
   return __uint_as_float(e == 0 ? v.x : (e == 1 ? v.y : (e == 2 ? v.z : v.w)));
 }
 
-template <typename T>
-__global__ void __launch_bounds__(kDraftThreads, 3) draft_topk_kernel(DraftArgs a) {
+// NW warps per CTA, NVL 16-byte vectors per lane and segment.
+template <typename T, int NW, int NVL>
+__global__ void __launch_bounds__(NW * 32, NW <= 8 ? 3 : 1) draft_topk_kernel(DraftArgs a) {
   using VT = VecTraits<T>;
   constexpr int VEC = VT::kElems;
-  constexpr int NVL = kDraftVecPerLane;
-  constexpr int SEG = 32 * NVL * VEC;  // tokens per warp
-  constexpr int NW = kDraftThreads / 32;
-  __shared__ uint64_t s_buf[NW][32 * 4];  // gathered keys of the block merge (NW*k, or S*k in the split merge)
-  __shared__ uint64_t s_wl[NW][32], s_tmp[NW][32];
-  __shared__ int s_wn[NW];
+  constexpr int SEG = 32 * NVL * VEC;  // tokens per warp and segment
+  constexpr int NT = NW * 32;
+  __shared__ __align__(16) uint64_t s_buf[NW][kBatchCap];  // a warp's candidates of one segment
+  __shared__ __align__(16) uint64_t s_wl[NW][32];           // a warp's list for its batch merge
+  __shared__ __align__(16) uint64_t s_tmp[NW][32];
+  __shared__ __align__(16) uint64_t s_all[NW * 32];          // the warps' lists: k slots each
+  // keys at or above a bound: at most NW*k (block merge) or S*k (part merge)
+  __shared__ __align__(16) uint64_t s_cand[(NW > kMaxDraftParts ? NW : kMaxDraftParts) * 32];
+  __shared__ __align__(16) uint64_t s_part_keys[kMaxDraftParts][32];  // first CTA: every part's top k
+  __shared__ float2 s_part_ms[kMaxDraftParts];                       // first CTA: every part's (max, sum)
+  __shared__ __align__(8) uint64_t s_part_bar;                      // first CTA: the parts have pushed
   __shared__ uint64_t s_top[32];
   __shared__ float s_m[NW], s_s[NW];
-  __shared__ int s_last;
+  __shared__ int s_nc;
   __shared__ unsigned s_thr;  // block prune bound (order-preserving bits)
 
-  const int s = blockIdx.x;
   const int rg = blockIdx.y;  // b * R + r
   const int b = rg / a.R, r = rg % a.R;
   const int d = r == 0 ? 0 : 1 + (r - 1) / a.k;
   const int j = r == 0 ? 0 : (r - 1) % a.k;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = a.k;
+  const int part = a.S > 1 ? static_cast<int>(cluster_ctarank()) : 0;
 
   const T *row = reinterpret_cast<const T *>(a.logits) +
                  ((static_cast<int64_t>(b) * a.D + d) * a.k + j) * a.ld;
-  if (tid == 0) s_thr = ordered_u32(-INFINITY);
-  if (lane == 0) s_wn[warp] = 0;
-  pdl_wait();
-  __syncthreads();  // s_thr and list sizes initialised
-  // This CTA's part of the row is a range of 2048-token segments (1024 for
-  // fp32); warp w takes segments w, w+8, ...  A segment is held in
-  // registers (all 16-byte loads in flight together) and visited twice:
-  // lane maxima, then the sum of exp(x - segment lane max).
+  // This CTA's part of the row is a range of segments; warp w takes
+  // segments w, w+NW, ...  A segment is held in registers (all 16-byte
+  // loads in flight together) and visited twice: lane maxima, then the sum
+  // of exp(x - segment lane max).
   const int nseg = (a.V + SEG - 1) / SEG;
   const int spp = (nseg + a.S - 1) / a.S;
-  const int g0 = s * spp, g1 = min(nseg, g0 + spp);
+  const int g0 = part * spp, g1 = min(nseg, g0 + spp);
+  uint4 vb[NVL];
+  auto load_segment = [&](int gseg) {
+    const int seg0 = gseg * SEG;
+    const int nvec = min(SEG, a.V - seg0) / VEC;
+#pragma unroll
+    for (int i = 0; i < NVL; ++i) {
+      const int v = lane + 32 * i;
+      if (v < nvec) vb[i] = ld_stream16(row + seg0 + v * VEC);
+    }
+  };
+  pdl_wait();
+  if (g0 + warp < g1) load_segment(g0 + warp);  // in flight while the shared state is set up
+  if (tid == 0) {
+    s_thr = ordered_u32(-INFINITY);
+    s_nc = 0;
+    if (a.S > 1) {
+      // the other parts' keys and (max, sum) arrive as transaction bytes
+      mbar_init(&s_part_bar, 1);
+      mbar_init_fence();
+      if (part == 0) sm100::mbar_arrive_expect_tx(&s_part_bar, (a.S - 1) * (k * 8 + 8));
+    }
+  }
+  if (tid < 32) s_top[tid] = 0ull;
+  __syncthreads();
+  if (a.S > 1) cluster_arrive_relaxed();  // waited on before a part pushes to the first CTA
+
   float m = -INFINITY, sum = 0.f;  // this lane's running max and sum of exp(x - m)
   float lmax = -INFINITY;          // this lane's largest value so far
   float thr = -INFINITY;           // prune bound: at least k values of the part are >= thr
@@ -142,24 +182,33 @@ __global__ void __launch_bounds__(kDraftThreads, 3) draft_topk_kernel(DraftArgs 
       if (cnt == k) thr = fmaxf(thr, key_value(shfl_u64(mine, k - 1)));
     }
   };
-  for (int gseg = g0 + warp; gseg < g1; gseg += NW) {
+  float M = -INFINITY, Z = 0.f;  // the part's softmax statistics (warp 0)
+  if constexpr (NW == 16) {
+    // ---- one segment per warp: selection against one block-wide bound ----
+    // Warp w has k distinct elements (lane maxima) at or above its k-th
+    // largest lane maximum, so the largest of these over the warps, T,
+    // bounds the part's k-th largest value from below.  Every element at or
+    // above T is gathered (one shared atomic per warp) and the gathered keys
+    // are ranked by counting.  A flat row with more than kGatherCap such
+    // elements takes the per-warp lists instead.
+    constexpr int kGatherCap = 256;
+    const int gseg = g0 + warp;
+    const bool has = gseg < g1;  // warp-uniform
     const int seg0 = gseg * SEG;
-    const int nvec = min(SEG, a.V - seg0) / VEC;
-    uint4 vb[NVL];
-#pragma unroll
-    for (int i = 0; i < NVL; ++i) {
-      const int v = lane + 32 * i;
-      if (v < nvec) vb[i] = ld_stream16(row + seg0 + v * VEC);
-    }
-    float smax = -INFINITY;
+    const int nvec = has ? min(SEG, a.V - seg0) / VEC : 0;
     float vmx[NVL];
+    float smax = -INFINITY;
 #pragma unroll
     for (int i = 0; i < NVL; ++i) {
       vmx[i] = (lane + 32 * i < nvec) ? vec_max<T>(vb[i]) : -INFINITY;
       smax = fmaxf(smax, vmx[i]);
     }
+    if (has) {
+      const float y = warp_sort_desc(smax, lane);
+      const float kth = __shfl_sync(0xffffffffu, y, k - 1);
+      if (lane == 0 && kth > -INFINITY) atomicMax(&s_thr, ordered_u32(kth));
+    }
     if (smax > -INFINITY) {
-      // sum of 2^(x*log2e - smax*log2e): per element one extract, FMA, ex2, add
       const float nmL = -smax * kLog2e;
       float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
@@ -174,230 +223,416 @@ __global__ void __launch_bounds__(kDraftThreads, 3) draft_topk_kernel(DraftArgs 
           }
         }
       }
-      lse_combine(m, sum, smax, acc0 + acc1);
+      m = smax;
+      sum = acc0 + acc1;
     }
-    lmax = fmaxf(lmax, smax);
-    // prune bound: before the list holds k keys, the k-th largest lane
-    // maximum (lane maxima are distinct elements); the block's shared
-    // maximum of its warps' bounds every segment (one shared load)
-    if (cnt < k) {
-      const float y = warp_sort_desc(lmax, lane);
-      thr = fmaxf(thr, __shfl_sync(0xffffffffu, y, k - 1));
+    pdl_trigger();
+    {
+      const float mw = warp_max(m);
+      const float sw = warp_sum((m == -INFINITY) ? 0.f : sum * ex2_approx((m - mw) * kLog2e));
+      if (lane == 0) {
+        s_m[warp] = mw;
+        s_s[warp] = sw;
+      }
     }
-    thr = fmaxf(thr, from_ordered_u32(*const_cast<volatile unsigned *>(&s_thr)));
-    if (!__any_sync(0xffffffffu, smax > -INFINITY && smax >= thr)) continue;
-    unsigned cms[NVL];  // this lane's elements of each vector at or above the bound
+    __syncthreads();
+    const float bound = from_ordered_u32(s_thr);
+    unsigned cms[NVL];
     int mycnt = 0;
 #pragma unroll
     for (int i = 0; i < NVL; ++i) {
       cms[i] = 0;
-      if (vmx[i] > -INFINITY && vmx[i] >= thr) {
+      if (vmx[i] > -INFINITY && vmx[i] >= bound) {
         float x[VEC];
         VT::unpack(vb[i], x);
 #pragma unroll
         for (int e = 0; e < VEC; ++e)
-          if (x[e] >= thr && x[e] > -INFINITY) cms[i] |= 1u << e;
+          if (x[e] >= bound && x[e] > -INFINITY) cms[i] |= 1u << e;
       }
       mycnt += __popc(cms[i]);
     }
-    const int total = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(mycnt)));
-    if (total > 4 && total <= kBatchCap) {
-      // many candidates (a warp's first segment): write them to the warp's
-      // buffer, then keep the k best of list + buffer by rank counting
-      int pos = mycnt;
+    int pos = mycnt;  // inclusive prefix over the lanes, then exclusive
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, pos, o);
-        if (lane >= o) pos += v;
-      }
-      pos -= mycnt;
-      uint64_t *buf = s_buf[warp];
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, pos, o);
+      if (lane >= o) pos += v;
+    }
+    const int total = __shfl_sync(0xffffffffu, pos, 31);
+    pos -= mycnt;
+    int base = 0;
+    if (lane == 0 && total > 0) base = atomicAdd(&s_nc, total);
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (base + total <= kGatherCap) {
 #pragma unroll
       for (int i = 0; i < NVL; ++i)
         for (unsigned cm = cms[i]; cm; cm &= cm - 1) {
           const int e = __ffs(cm) - 1;
-          buf[pos++] = topk_key(elem_of<T>(vb[i], e), static_cast<uint32_t>(seg0 + (lane + 32 * i) * VEC + e));
+          s_cand[base + pos++] = topk_key(elem_of<T>(vb[i], e), static_cast<uint32_t>(seg0 + (lane + 32 * i) * VEC + e));
         }
-      if (lane < cnt) s_wl[warp][lane] = mine;
-      __syncwarp();
-      for (int q = lane; q < cnt + total; q += 32) {
-        const uint64_t key = q < cnt ? s_wl[warp][q] : buf[q - cnt];
-        const int rk = rank_in(key, s_wl[warp], cnt) + rank_in(key, buf, total);
-        if (rk < k) s_tmp[warp][rk] = key;
+    }
+    if (warp == 0) {
+      const float mw = lane < NW ? s_m[lane] : -INFINITY;
+      M = warp_max(mw);
+      Z = warp_sum(mw == -INFINITY ? 0.f : s_s[lane] * ex2_approx((mw - M) * kLog2e));
+    }
+    __syncthreads();
+    const int nc = s_nc;
+    if (nc <= kGatherCap) {
+      for (int i = tid; i < nc; i += NT) {
+        const uint64_t key = s_cand[i];
+        const int rk = count_greater(key, s_cand, nc);
+        if (rk < k) s_top[rk] = key;
       }
-      __syncwarp();
-      cnt = cnt + total < k ? cnt + total : k;
-      mine = lane < cnt ? s_tmp[warp][lane] : 0ull;
-      if (cnt == k) thr = fmaxf(thr, key_value(shfl_u64(mine, k - 1)));
-      __syncwarp();
     } else {
+      // flat row: each warp keeps its k best of the gathered elements in
+      // registers (one ballot-ranked insert per element), then the NW lists
+      // are ranked together
 #pragma unroll
-    for (int i = 0; i < NVL; ++i) {
-      unsigned cm = cms[i];
-      // insert them one by one (lowest lane, lowest element first); each
-      // insert may raise the bound and drop later ones
-      for (unsigned lanes = __ballot_sync(0xffffffffu, cm != 0); lanes;
-           lanes = __ballot_sync(0xffffffffu, cm != 0)) {
-        const int src = __ffs(lanes) - 1;
-        uint64_t key = 0;
-        if (lane == src) {
-          const int e = __ffs(cm) - 1;
-          cm &= cm - 1;
-          key = topk_key(elem_of<T>(vb[i], e), static_cast<uint32_t>(seg0 + (lane + 32 * i) * VEC + e));
+      for (int i = 0; i < NVL; ++i) {
+        unsigned cm = cms[i];
+        for (unsigned lanes = __ballot_sync(0xffffffffu, cm != 0); lanes;
+             lanes = __ballot_sync(0xffffffffu, cm != 0)) {
+          const int src = __ffs(lanes) - 1;
+          uint64_t key = 0;
+          if (lane == src) {
+            const int e = __ffs(cm) - 1;
+            cm &= cm - 1;
+            key = topk_key(elem_of<T>(vb[i], e), static_cast<uint32_t>(seg0 + (lane + 32 * i) * VEC + e));
+          }
+          insert(shfl_u64(key, src));
         }
-        key = shfl_u64(key, src);
-        if (key_value(key) >= thr) insert(key);
-        if (cm && !(vmx[i] >= thr)) cm = 0;  // the raised bound excludes the rest of this vector
+      }
+      if (lane < k) s_all[warp * k + lane] = mine;
+      __syncthreads();
+      for (int i = tid; i < NW * k; i += NT) {
+        const uint64_t key = s_all[i];
+        if (!key) continue;
+        const int rk = count_greater(key, s_all, NW * k);
+        if (rk < k) s_top[rk] = key;
       }
     }
+    __syncthreads();
+  } else {
+    for (int gseg = g0 + warp; gseg < g1; gseg += NW) {
+      if (gseg != g0 + warp) load_segment(gseg);
+      const int seg0 = gseg * SEG;
+      const int nvec = min(SEG, a.V - seg0) / VEC;
+      float smax = -INFINITY;
+      float vmx[NVL];
+  #pragma unroll
+      for (int i = 0; i < NVL; ++i) {
+        vmx[i] = (lane + 32 * i < nvec) ? vec_max<T>(vb[i]) : -INFINITY;
+        smax = fmaxf(smax, vmx[i]);
+      }
+      if (smax > -INFINITY) {
+        // sum of 2^(x*log2e - smax*log2e): per element one extract, FMA, ex2, add
+        const float nmL = -smax * kLog2e;
+        float acc0 = 0.f, acc1 = 0.f;
+  #pragma unroll
+        for (int i = 0; i < NVL; ++i) {
+          if (lane + 32 * i < nvec) {
+            float x[VEC];
+            VT::unpack(vb[i], x);
+  #pragma unroll
+            for (int e = 0; e < VEC; e += 2) {
+              acc0 += ex2_approx(fmaf(x[e], kLog2e, nmL));
+              acc1 += ex2_approx(fmaf(x[e + 1], kLog2e, nmL));
+            }
+          }
+        }
+        lse_combine(m, sum, smax, acc0 + acc1);
+      }
+      lmax = fmaxf(lmax, smax);
+      // prune bound: before the list holds k keys, the k-th largest lane
+      // maximum (lane maxima are distinct elements); the block's shared
+      // maximum of its warps' bounds every segment (one shared load)
+      if (cnt < k) {
+        const float y = warp_sort_desc(lmax, lane);
+        thr = fmaxf(thr, __shfl_sync(0xffffffffu, y, k - 1));
+      }
+      thr = fmaxf(thr, from_ordered_u32(*const_cast<volatile unsigned *>(&s_thr)));
+      if (!__any_sync(0xffffffffu, smax > -INFINITY && smax >= thr)) continue;
+      unsigned cms[NVL];  // this lane's elements of each vector at or above the bound
+      int mycnt = 0;
+  #pragma unroll
+      for (int i = 0; i < NVL; ++i) {
+        cms[i] = 0;
+        if (vmx[i] > -INFINITY && vmx[i] >= thr) {
+          float x[VEC];
+          VT::unpack(vb[i], x);
+  #pragma unroll
+          for (int e = 0; e < VEC; ++e)
+            if (x[e] >= thr && x[e] > -INFINITY) cms[i] |= 1u << e;
+        }
+        mycnt += __popc(cms[i]);
+      }
+      const int total = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(mycnt)));
+      if (total > 4 && total <= kBatchCap) {
+        // many candidates (a warp's first segment): write them to the warp's
+        // buffer, then keep the k best of list + buffer by counting larger keys
+        int pos = mycnt;
+  #pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, pos, o);
+          if (lane >= o) pos += v;
+        }
+        pos -= mycnt;
+        uint64_t *buf = s_buf[warp];
+  #pragma unroll
+        for (int i = 0; i < NVL; ++i)
+          for (unsigned cm = cms[i]; cm; cm &= cm - 1) {
+            const int e = __ffs(cm) - 1;
+            buf[pos++] = topk_key(elem_of<T>(vb[i], e), static_cast<uint32_t>(seg0 + (lane + 32 * i) * VEC + e));
+          }
+        if (lane < cnt) s_wl[warp][lane] = mine;
+        __syncwarp();
+        for (int q = lane; q < cnt + total; q += 32) {
+          const uint64_t key = q < cnt ? s_wl[warp][q] : buf[q - cnt];
+          const int rk = count_greater(key, s_wl[warp], cnt) + count_greater(key, buf, total);
+          if (rk < k) s_tmp[warp][rk] = key;
+        }
+        __syncwarp();
+        cnt = cnt + total < k ? cnt + total : k;
+        mine = lane < cnt ? s_tmp[warp][lane] : 0ull;
+        if (cnt == k) thr = fmaxf(thr, key_value(shfl_u64(mine, k - 1)));
+        __syncwarp();
+      } else {
+  #pragma unroll
+      for (int i = 0; i < NVL; ++i) {
+        unsigned cm = cms[i];
+        // insert them one by one (lowest lane, lowest element first); each
+        // insert may raise the bound and drop later ones
+        for (unsigned lanes = __ballot_sync(0xffffffffu, cm != 0); lanes;
+             lanes = __ballot_sync(0xffffffffu, cm != 0)) {
+          const int src = __ffs(lanes) - 1;
+          uint64_t key = 0;
+          if (lane == src) {
+            const int e = __ffs(cm) - 1;
+            cm &= cm - 1;
+            key = topk_key(elem_of<T>(vb[i], e), static_cast<uint32_t>(seg0 + (lane + 32 * i) * VEC + e));
+          }
+          key = shfl_u64(key, src);
+          if (key_value(key) >= thr) insert(key);
+          if (cm && !(vmx[i] >= thr)) cm = 0;  // the raised bound excludes the rest of this vector
+        }
+      }
+      }
+      if (cnt == k && thr > published) {  // raise the block's bound (rare once warm)
+        if (lane == 0) atomicMax(&s_thr, ordered_u32(thr));
+        published = thr;
+      }
     }
-    if (cnt == k && thr > published) {  // raise the block's bound (rare once warm)
-      if (lane == 0) atomicMax(&s_thr, ordered_u32(thr));
-      published = thr;
-    }
-  }
-  if (lane < k) s_wl[warp][lane] = mine;
-  if (lane == 0) s_wn[warp] = cnt;
-  pdl_trigger();
+    // this warp's list into its k slots (empty slots hold zero keys)
+    if (lane < k) s_all[warp * k + lane] = mine;
+    pdl_trigger();
 
-  // ---- block: softmax statistics and the top k of the warp lists ------------
-  {
-    float mw = warp_max(m);
-    float sw = (m == -INFINITY) ? 0.f : sum * ex2_approx((m - mw) * kLog2e);
-    sw = warp_sum(sw);
-    if (lane == 0) {
-      s_m[warp] = mw;
-      s_s[warp] = sw;
+    // ---- block: softmax statistics and the top k of the warp lists ------------
+    {
+      const float mw = warp_max(m);
+      const float sw = warp_sum((m == -INFINITY) ? 0.f : sum * ex2_approx((m - mw) * kLog2e));
+      if (lane == 0) {
+        s_m[warp] = mw;
+        s_s[warp] = sw;
+      }
     }
+    __syncthreads();
+    // The top k of the block are among the keys at or above a lower bound
+    // for its k-th largest key: the larger of the block's prune bound and the
+    // k-th largest of a sample holding each warp's best ceil(k/NW) keys (at
+    // least k keys of the block reach either).  The warps that gather the
+    // keys at or above it each compute the sample bound themselves; the
+    // gathered keys are then ranked by counting.
+    static_assert(NW <= 32 && (NW & (NW - 1)) == 0, "NW * ceil(k/NW) <= 32 for every k <= 32");
+    const int per_w = (k + NW - 1) / NW;
+    if (warp * 32 < NW * k) {
+      float sv = -INFINITY;
+      if (lane < NW * per_w) {
+        const uint64_t key = s_all[(lane / per_w) * k + lane % per_w];
+        if (key) sv = key_value(key);
+      }
+      const float y = warp_sort_desc(sv, lane);
+      const float bound = fmaxf(__shfl_sync(0xffffffffu, y, k - 1), from_ordered_u32(s_thr));
+      const uint64_t key = tid < NW * k ? s_all[tid] : 0ull;
+      const bool in = key && key_value(key) >= bound;
+      const unsigned bal = __ballot_sync(0xffffffffu, in);
+      int base = 0;
+      if (lane == 0 && bal) base = atomicAdd(&s_nc, __popc(bal));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      if (in) s_cand[base + __popc(bal & ((1u << lane) - 1u))] = key;
+    }
+    // the warps' (max, sum) pairs combined by one warp: the block maximum,
+    // then each pair rescaled to it (one exponential per lane) and summed
+    if (warp == 0) {
+      const float mw = lane < NW ? s_m[lane] : -INFINITY;
+      M = warp_max(mw);
+      Z = warp_sum(mw == -INFINITY ? 0.f : s_s[lane] * ex2_approx((mw - M) * kLog2e));
+    }
+    __syncthreads();
+    const int nc = s_nc;
+    for (int i = tid; i < nc; i += NT) {
+      const uint64_t key = s_cand[i];
+      const int rk = count_greater(key, s_cand, nc);
+      if (rk < k) s_top[rk] = key;
+    }
+    __syncthreads();
   }
-  __syncthreads();
-  // gather the warp lists into one array (the first warp's buffer)
-  uint64_t *U = s_buf[0];
-  int C = 0;
-  for (int w = 0; w < NW; ++w) {
-    const int nw = s_wn[w];
-    if (tid < nw) U[C + tid] = s_wl[w][tid];
-    C += nw;
-  }
-  if (tid < 32) s_top[tid] = 0ull;
-  __syncthreads();
-  for (int i = tid; i < C; i += kDraftThreads) {
-    const uint64_t key = U[i];
-    const int rk = rank_in(key, U, C);
-    if (rk < k) s_top[rk] = key;
-  }
-  float M = s_m[0], Z = s_s[0];
-  for (int w = 1; w < NW; ++w) lse_combine(M, Z, s_m[w], s_s[w]);
-  __syncthreads();
 
   const int64_t slot = ((static_cast<int64_t>(b) * a.D + d) * a.k + j);
-  auto finalize = [&](const uint64_t *top, float Mf, float Zf) {
-    if (tid < k) {
-      const uint64_t key = top[tid];
+  auto finalize = [&](const uint64_t *top, float Mf, float Zf) {  // by warp 0
+    if (lane < k) {
+      const uint64_t key = top[lane];
       int32_t t = -1;
       float cf = 0.f;
       if (key) {
         t = static_cast<int32_t>(key_token(key));
         cf = expf(key_value(key) - Mf) / Zf;
       }
-      a.tok[slot * a.k + tid] = t;
-      a.conf[slot * a.k + tid] = cf;
+      a.tok[slot * a.k + lane] = t;
+      a.conf[slot * a.k + lane] = cf;
     }
-    if (tid == 0 && a.stats) {
+    if (lane == 0 && a.stats) {
       a.stats[slot * 2 + 0] = Mf;
       a.stats[slot * 2 + 1] = logf(Zf);
     }
   };
   if (a.S == 1) {
-    finalize(s_top, M, Z);
+    if (warp == 0) finalize(s_top, M, Z);
     return;
   }
 
-  // ---- split rows: publish the partial, the last CTA merges ---------------
-  uint32_t *counters = reinterpret_cast<uint32_t *>(a.ws);
-  float2 *parts_ms = reinterpret_cast<float2 *>(a.ws + draft_counter_bytes(a.B, a.R));
-  uint64_t *parts_keys =
-      reinterpret_cast<uint64_t *>(a.ws + draft_counter_bytes(a.B, a.R) + draft_ms_bytes(a.B, a.R, a.S));
-  const int64_t prow = static_cast<int64_t>(rg) * a.S;
-  if (tid < k) parts_keys[(prow + s) * k + tid] = s_top[tid];
-  if (tid == 0) parts_ms[prow + s] = make_float2(M, Z);
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = (atomicAdd(counters + rg, 1u) == static_cast<uint32_t>(a.S - 1));
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-
-  const int CS = a.S * k;
-  for (int i = tid; i < CS; i += kDraftThreads)
-    U[i] = __ldcg(reinterpret_cast<const unsigned long long *>(parts_keys + prow * k + i));
-  if (tid < 32) s_top[tid] = 0ull;
-  __syncthreads();
-  for (int i = tid; i < CS; i += kDraftThreads) {
-    const uint64_t key = U[i];
-    if (!key) continue;  // a slice with fewer than k finite values
-    const int rk = rank_in(key, U, CS);
-    if (rk < k) s_top[rk] = key;
+  // ---- parts of a row: push to the first CTA of the cluster, which merges --
+  if (part != 0) {
+    cluster_wait();  // the first CTA's barrier is initialised
+    if (warp == 0) {
+      // asynchronous stores into the first CTA, each completing its share
+      // of the barrier's expected bytes
+      const uint32_t bar = mapa_shared(smem_u32(&s_part_bar), 0);
+      if (lane < k) {
+        const uint32_t dst = mapa_shared(smem_u32(&s_part_keys[part][lane]), 0);
+        const uint64_t key = s_top[lane];
+        asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];"
+                     ::"r"(dst), "l"(key), "r"(bar) : "memory");
+      }
+      if (lane == 0) {
+        const uint32_t dst = mapa_shared(smem_u32(&s_part_ms[part]), 0);
+        asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
+                     ::"r"(dst), "f"(M), "f"(Z), "r"(bar) : "memory");
+      }
+    }
+    return;
   }
+  cluster_wait();
   if (warp == 0) {
-    float pm = -INFINITY, ps = 0.f;
-    for (int q = lane; q < a.S; q += 32) {
-      const float2 ms = __ldcg(parts_ms + prow + q);
-      lse_combine(pm, ps, ms.x, ms.y);
-    }
-    const float Mw = warp_max(pm);
-    const float Zw = warp_sum(pm == -INFINITY ? 0.f : ps * ex2_approx((pm - Mw) * kLog2e));
-    if (lane == 0) {
-      s_m[0] = Mw;
-      s_s[0] = Zw;
+    bool ok = true;
+    if (lane == 0) ok = mbar_wait_cluster(&s_part_bar, 0, 200000000ull);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    if (!ok) {
+      if (lane == 0) report(a.status, EAGLE_ERR_TIMEOUT);
+    } else {
+      // own top k and (max, sum) as part 0, then the S*k keys ranked
+      if (lane < k) s_part_keys[0][lane] = s_top[lane];
+      float pm = lane == 0 ? M : -INFINITY, ps = lane == 0 ? Z : 0.f;
+      if (lane > 0 && lane < a.S) {
+        pm = s_part_ms[lane].x;
+        ps = s_part_ms[lane].y;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, pm, o), z2 = __shfl_xor_sync(0xffffffffu, ps, o);
+        lse_combine(pm, ps, m2, z2);
+      }
+      __syncwarp();
+      // candidates: keys at or above the largest k-th key of any part
+      float pb = -INFINITY;
+      for (int q = lane; q < a.S; q += 32) {
+        const uint64_t kth = s_part_keys[q][k - 1];
+        if (kth) pb = fmaxf(pb, key_value(kth));
+      }
+      pb = warp_max(pb);
+      int n = 0;
+      for (int q = 0; q < a.S; ++q) {
+        const uint64_t key = lane < k ? s_part_keys[q][lane] : 0ull;
+        const bool in = key && key_value(key) >= pb;
+        const unsigned bal = __ballot_sync(0xffffffffu, in);
+        if (in) s_cand[n + __popc(bal & ((1u << lane) - 1u))] = key;
+        n += __popc(bal);
+      }
+      if (lane < k) s_tmp[0][lane] = 0ull;
+      __syncwarp();
+      for (int q = lane; q < n; q += 32) {
+        const uint64_t key = s_cand[q];
+        const int rk = count_greater(key, s_cand, n);
+        if (rk < k) s_tmp[0][rk] = key;
+      }
+      __syncwarp();
+      finalize(s_tmp[0], pm, ps);
     }
   }
-  __syncthreads();
-  finalize(s_top, s_m[0], s_s[0]);
-  if (tid == 0) counters[rg] = 0;  // leave the ticket zeroed for the next call
 }
 
 // ---- host side ---------------------------------------------------------------
 
-// Parts (CTAs) per row: enough CTAs for about three per SM, but no part
-// smaller than one 2048-token segment per warp.
-int draft_splits(int B, int R, int V, int vec, int num_sms) {
+struct DraftPlan {
+  int NW, NVL, S;
+};
+
+// Few rows: 16-warp CTAs with 1024-token segments (bf16), when each row can
+// be split into parts of one segment per warp with every part resident at
+// once (one CTA per SM).  Otherwise 8-warp CTAs with 2048-token segments:
+// enough parts for about three CTAs per SM, but no part smaller than one
+// segment per warp.  At most kMaxDraftParts parts per row (one cluster).
+static DraftPlan draft_plan(int B, int R, int V, int vec, int num_sms) {
   const int64_t rows = static_cast<int64_t>(B) * R;
-  const int seg = kDraftVecPerLane * 32 * vec;
+  DraftPlan p;
+  {
+    const int seg = 4 * 32 * vec;
+    const int64_t nseg = (V + seg - 1) / seg;
+    const int64_t parts = (nseg + 15) / 16;
+    if (parts <= kMaxDraftParts && rows * parts <= num_sms) {
+      p.NW = 16;
+      p.NVL = 4;
+      p.S = static_cast<int>(parts);
+      return p;
+    }
+  }
+  const int seg = 8 * 32 * vec;
   const int64_t nseg = (V + seg - 1) / seg;
-  const int64_t max_parts = (nseg + (kDraftThreads / 32) - 1) / (kDraftThreads / 32);
+  const int64_t max_parts = (nseg + 7) / 8;
   int64_t S = (static_cast<int64_t>(num_sms) * 3 + rows - 1) / rows;
   if (S > max_parts) S = max_parts;
-  if (S > 32) S = 32;
+  if (S > kMaxDraftParts) S = kMaxDraftParts;
   if (S < 1) S = 1;
-  return static_cast<int>(S);
+  p.NW = 8;
+  p.NVL = 8;
+  p.S = static_cast<int>(S);
+  return p;
 }
 
-size_t draft_workspace_bytes(int B, int D, int k, int V, int vec, int num_sms) {
-  const int R = 1 + (D - 1) * k;
-  const int S = draft_splits(B, R, V, vec, num_sms);
-  if (S == 1) return draft_counter_bytes(B, R);
-  return draft_counter_bytes(B, R) + draft_ms_bytes(B, R, S) + static_cast<size_t>(B) * R * S * k * sizeof(uint64_t);
-}
+// The parts of a row merge through the shared memory of their cluster: no
+// workspace.
+size_t draft_workspace_bytes(int, int, int, int, int, int) { return 0; }
 
 template <typename T>
-static cudaError_t launch_t(const DraftArgs &a, cudaStream_t st) {
-  return launch_chained(draft_topk_kernel<T>, dim3(a.S, a.B * a.R), dim3(kDraftThreads), 0, st, a);
+static cudaError_t launch_t(const DraftArgs &a, const DraftPlan &p, cudaStream_t st) {
+  const dim3 grid(a.S, a.B * a.R);
+  if (p.NW == 16)
+    return launch_chained_cluster(draft_topk_kernel<T, 16, 4>, grid, dim3(16 * 32), 0, st, a.S, a);
+  return launch_chained_cluster(draft_topk_kernel<T, 8, 8>, grid, dim3(8 * 32), 0, st, a.S, a);
 }
 
 cudaError_t launch_draft_topk(const void *logits, int dtype, int B, int D, int k, int V,
                               int64_t ld, int32_t *tok, float *conf, float *stats,
-                              void *ws, int32_t *status, int num_sms, cudaStream_t st) {
+                              void *, int32_t *status, int num_sms, cudaStream_t st) {
   DraftArgs a;
   a.logits = logits;
   a.B = B; a.D = D; a.k = k; a.V = V; a.ld = ld;
   a.R = 1 + (D - 1) * k;
   const int vec = dtype == EAGLE_BF16 ? 8 : 4;
-  a.S = draft_splits(B, a.R, V, vec, num_sms);
+  const DraftPlan p = draft_plan(B, a.R, V, vec, num_sms);
+  a.S = p.S;
   a.tok = tok; a.conf = conf; a.stats = stats;
-  a.ws = reinterpret_cast<unsigned char *>(ws);
   a.status = status;
-  return dtype == EAGLE_BF16 ? launch_t<__nv_bfloat16>(a, st) : launch_t<float>(a, st);
+  return dtype == EAGLE_BF16 ? launch_t<__nv_bfloat16>(a, p, st) : launch_t<float>(a, p, st);
 }
 
 }  // namespace eagle

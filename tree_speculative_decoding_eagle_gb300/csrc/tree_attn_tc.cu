@@ -84,7 +84,9 @@ struct TcShape {
 // Most KV splits of one (sequence, KV head, M-group): one cluster of CTAs.
 constexpr int kMaxClusterSplits = 8;
 
-template <int DH, int MT, int NK, int STAGES>
+// SPLIT: the grid splits the KV range (S > 1) and the kernel carries the
+// cluster merge; without it the merge code is compiled out.
+template <int DH, int MT, int NK, int STAGES, bool SPLIT>
 __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
     tree_attn_tc_kernel(const __grid_constant__ CUtensorMap kc_map, const __grid_constant__ CUtensorMap vc_map,
                         const __grid_constant__ CUtensorMap kt_map, const __grid_constant__ CUtensorMap vt_map,
@@ -161,8 +163,10 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
     mbar_init(&turn[0], 4);
     mbar_init(&turn[1], 4);
     mbar_init(q_full, 1);
-    mbar_init(cl_full, a.S);
-    mbar_init(cl_done, a.S);
+    if constexpr (SPLIT) {
+      mbar_init(cl_full, a.S);
+      mbar_init(cl_done, a.S);
+    }
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -173,7 +177,7 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (a.S > 1) cluster_arrive_relaxed();  // waited on before the first signal to a peer
+  if constexpr (SPLIT) cluster_arrive_relaxed();  // waited on before the first signal to a peer
   const uint32_t tmem = *tmem_slot;
 
   int issued = 0;  // producer: tiles issued
@@ -184,7 +188,7 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
   if (warp == producer_warp) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
-      if (a.q_tma && T > 0) {
+      if (a.q_tma) {
         mbar_arrive_expect_tx(q_full, MT * Sh::kRegions * 16384);
         for (int t = 0; t < MT; ++t)
 #pragma unroll
@@ -409,19 +413,26 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
       const float nb = base > -INFINITY ? -base : 0.f;
       const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2), nb2 = f2_pack(nb, nb);
       uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
+      // packed P in two 16-column pieces, so only one piece's registers are
+      // live next to the scores
       auto exp_half = [&](int h, const float (&sv)[64]) {
-        float pk[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          float t0, t1;
-          f2_unpack(f2_fma(f2_pack(sv[2 * c], sv[2 * c + 1]), sc2, nb2), t0, t1);
-          const float p0v = ex2_approx(t0), p1v = ex2_approx(t1);
-          if (c & 1) acc1 = f2_add(acc1, f2_pack(p0v, p1v));
-          else acc0 = f2_add(acc0, f2_pack(p0v, p1v));
-          __nv_bfloat162 h2 = __floats2bfloat162_rn(p0v, p1v);
-          pk[c] = *reinterpret_cast<const float *>(&h2);
+        for (int q = 0; q < 2; ++q) {
+          float pk[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const int cc = 16 * q + c;
+            float t0, t1;
+            f2_unpack(f2_fma(f2_pack(sv[2 * cc], sv[2 * cc + 1]), sc2, nb2), t0, t1);
+            const float p0v = ex2_approx(t0), p1v = ex2_approx(t1);
+            if (c & 1) acc1 = f2_add(acc1, f2_pack(p0v, p1v));
+            else acc0 = f2_add(acc0, f2_pack(p0v, p1v));
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(p0v, p1v);
+            pk[c] = *reinterpret_cast<const float *>(&h2);
+          }
+          tmem_st16_async(tP + 32 * h + 16 * q, pk);
         }
-        tmem_st32(tP + 32 * h, pk);
+        tmem_wait_st();
       };
       if constexpr (NH == 1) {
         exp_half(0, sv0);
@@ -459,19 +470,19 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
     }
     if (ok && T > 0 && !warp_wait(&o_done[t], (T - 1) & 1, abort_flag)) ok = false;
     tc_fence_after();
+    // tcgen05.ld is warp-collective (.sync.aligned): every lane executes it,
+    // rows past the last node only skip the global writes
+    const int h = g * a.G + hh;
+    const int64_t orow = (static_cast<int64_t>(b) * n + i) * a.Hq + h;
     const bool have = ok && T > 0;
-    if (a.S > 1) {
+    const float inv = (have && l > 0.f) ? 1.f / l : 0.f;
+    if constexpr (SPLIT) {
       // split: (m, l) wait for the cluster merge; O stays in tensor memory
       // until every MMA of the CTA is done (the teardown barrier)
       part_have = have;
       part_m = m;
       part_l = l;
     } else {
-      // tcgen05.ld is warp-collective (.sync.aligned): every lane executes
-      // it, rows past the last node only skip the global writes
-      const int h = g * a.G + hh;
-      const int64_t orow = (static_cast<int64_t>(b) * n + i) * a.Hq + h;
-      const float inv = (have && l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll
       for (int c0 = 0; c0 < DH; c0 += 32) {
         float o[32];
@@ -498,6 +509,10 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (a.q_tma && T == 0 && warp == producer_warp && lane == 0) {
+    volatile int never = 0;
+    mbar_wait(q_full, 0, &never, 100000000ull);  // nothing else waits for an empty split's Q copy
+  }
   if (*abort_flag) {
     if (tid == 0) report(a.status, EAGLE_ERR_TIMEOUT);
     volatile int never = 0;
@@ -514,7 +529,7 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
     }
     __syncthreads();
   }
-  if (a.S > 1 && warp < MT * 4) {
+  if (SPLIT && warp < MT * 4) {
     // this CTA's unnormalised O rows (fp32) into the stage buffers and its
     // (m, l) pairs into the Q buffer: every MMA and copy has completed.  Row
     // r's 16-byte chunk c sits at chunk c ^ (r & 7) of the row, so the 32
@@ -539,8 +554,10 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
     reinterpret_cast<float2 *>(sQ)[rl] = have ? make_float2(part_m * kLn2, part_l) : make_float2(-INFINITY, 0.f);
     fence_acq_rel_cluster();
   }
-  tc_fence_before();
-  __syncthreads();
+  if constexpr (SPLIT) {
+    tc_fence_before();
+    __syncthreads();
+  }
   if (warp == mma_warp) tmem_dealloc(tmem, Sh::kTmemCols);
 
   // ---- split merge across the cluster ----------------------------------------
@@ -551,7 +568,7 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
   // M = max_s m_s, L = sum_s exp(m_s - M) l_s.  A second round of signals
   // keeps every CTA's shared memory alive until its peers have read it.
   // Both waits are bounded; a timeout raises EAGLE_ERR_TIMEOUT.
-  if (a.S > 1) {
+  if constexpr (SPLIT) {
     cluster_wait();  // every peer has initialised its barriers
     const uint32_t rank = cluster_ctarank();
     if (tid < a.S) mbar_arrive_remote(mapa_shared(smem_u32(cl_full), tid));  // one peer per thread
@@ -720,23 +737,29 @@ static TcPlan tc_plan(int B, int n, int Hq, int Hkv, int dh, int Lmax, int num_s
 // The splits merge through distributed shared memory: no workspace.
 size_t attn_tc_workspace_bytes(int, int, int, int, int, int, int) { return 0; }
 
-template <int DH, int MT, int NK, int STAGES>
-static cudaError_t launch_tc_t(const CUtensorMap *maps, const TcArgs &a, const TcPlan &p, cudaStream_t st) {
+template <int DH, int MT, int NK, int STAGES, bool SPLIT>
+static cudaError_t launch_tc_v(const CUtensorMap *maps, const TcArgs &a, const TcPlan &p, cudaStream_t st) {
   using Sh = TcShape<DH, MT, NK, STAGES>;
   static_assert(Sh::kSmem <= 232448, "shared memory budget");
   // MT = 1 variants run two CTAs per SM (228 KB per SM, 1 KB reserved per CTA)
   static_assert(MT != 1 || 2 * (Sh::kSmem + 1024) <= 233472, "two CTAs per SM");
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(tree_attn_tc_kernel<DH, MT, NK, STAGES>,
+    cudaError_t e = cudaFuncSetAttribute(tree_attn_tc_kernel<DH, MT, NK, STAGES, SPLIT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   // the S splits of one (b, g, M-group) form one cluster
   dim3 grid(p.S, p.mgroups, a.B * a.Hkv);
-  return launch_chained_cluster(tree_attn_tc_kernel<DH, MT, NK, STAGES>, grid, dim3(Sh::kThreads), Sh::kSmem, st,
-                                p.S, maps[0], maps[1], maps[2], maps[3], maps[4], a);
+  return launch_chained_cluster(tree_attn_tc_kernel<DH, MT, NK, STAGES, SPLIT>, grid, dim3(Sh::kThreads), Sh::kSmem,
+                                st, p.S, maps[0], maps[1], maps[2], maps[3], maps[4], a);
+}
+
+template <int DH, int MT, int NK, int STAGES>
+static cudaError_t launch_tc_t(const CUtensorMap *maps, const TcArgs &a, const TcPlan &p, cudaStream_t st) {
+  return p.S > 1 ? launch_tc_v<DH, MT, NK, STAGES, true>(maps, a, p, st)
+                 : launch_tc_v<DH, MT, NK, STAGES, false>(maps, a, p, st);
 }
 
 // Common launcher; block_table == nullptr is the contiguous cache, otherwise
