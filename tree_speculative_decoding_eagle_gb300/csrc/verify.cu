@@ -14,9 +14,10 @@
 //      2048-token chunk of a row and records (max, sum exp(y - max), argmax)
 //      of y = x / T; these do not depend on the tree, so the pass can run
 //      beside the draft stages.
-//  (b) verify_walk: one warp per sequence walks the tree using the chunk
-//      statistics, a handful of single-logit reads for the children's tokens
-//      and, for a bonus draw, one re-read of a single chunk.
+//  (b) verify_walk: one CTA per sequence first loads, in one parallel round,
+//      every node's parent, token, logit in its parent's row and uniforms,
+//      and the sequence's chunk statistics; one warp then walks the tree
+//      from shared memory and, for a bonus draw, re-reads one chunk.
 #include "common.cuh"
 
 namespace eagle {
@@ -35,6 +36,7 @@ struct VerifyArgs {
   int64_t ld;
   const int32_t *node_tok, *node_parent;
   int B, m, n, D, V, nch, mode;
+  int stage_stats;  // walk: the sequence's chunk statistics are copied to shared memory first
   float inv_t;
   const float *u;
   int32_t *accept_len, *path_nodes, *out_tokens, *status;
@@ -128,31 +130,59 @@ __device__ __forceinline__ float logit_at(const VerifyArgs &a, int64_t row, int 
   return VecTraits<T>::load1(a.target, row * a.ld + t);
 }
 
+constexpr int kWalkThreads = 256;
+
+// The walk.  Every state the walk can visit is loaded first, by all eight
+// warps in one round: each node's parent and token, its logit in its
+// parent's row and its two uniforms (sampling), and the sequence's chunk
+// statistics (when they fit in shared memory).  Warp 0 then walks, reducing
+// the current row's chunk statistics at each step; only the sampling bonus
+// reads the target again (one chunk).
 template <typename T>
-__global__ void __launch_bounds__(32) verify_walk_kernel(VerifyArgs a) {
+__global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(VerifyArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
-  int *s_par = reinterpret_cast<int *>(smem);
-  int *s_tok = s_par + a.n;
-  int *s_rej = s_tok + a.n;  // rejected tokens at the current node
-  float *s_rej_e = reinterpret_cast<float *>(s_rej + a.n);  // and their exp terms
-  const int b = blockIdx.x;
-  const int lane = threadIdx.x;
   const int n = a.n;
+  ChunkStat *s_cs = reinterpret_cast<ChunkStat *>(smem);  // [n][nch] when staged
+  int *s_par = reinterpret_cast<int *>(smem + (a.stage_stats ? sizeof(ChunkStat) * n * a.nch : 0));
+  int *s_tok = s_par + n;
+  int *s_rej = s_tok + n;  // rejected tokens at the current node
+  float *s_rej_e = reinterpret_cast<float *>(s_rej + n);  // and their exp terms
+  float *s_x = s_rej_e + n;   // node i's logit in its parent's row (sampling)
+  float *s_u = s_x + n;       // [n][2] node i's uniforms (sampling)
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t nb = static_cast<int64_t>(b) * n;
   const float sc = a.inv_t * kLog2e;  // logit -> base-2 exponent of exp(x / T), as the statistics pass
-  pdl_wait();
-  for (int i = lane; i < n; i += 32) {
-    s_par[i] = a.node_parent[nb + i];
-    s_tok[i] = a.node_tok[nb + i];
-  }
-  __syncwarp();
   const bool sample = a.mode == EAGLE_SAMPLE;
+  pdl_wait();
+  if (a.stage_stats) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(a.stats + nb * a.nch);
+    uint4 *dst = reinterpret_cast<uint4 *>(s_cs);
+    const int total = n * a.nch;
+#pragma unroll 8
+    for (int q = tid; q < total; q += kWalkThreads) dst[q] = src[q];
+  }
+  for (int i = tid; i < n; i += kWalkThreads) {
+    const int par = a.node_parent[nb + i], tk = a.node_tok[nb + i];
+    s_par[i] = par;
+    s_tok[i] = tk;
+    if (sample) {
+      float x = 0.f;
+      if (i > 0 && par >= 0 && par < n && tk >= 0 && tk < a.V) x = logit_at<T>(a, nb + par, tk);
+      s_x[i] = x;
+      s_u[2 * i] = a.u[(nb + i) * 2 + 0];
+      s_u[2 * i + 1] = a.u[(nb + i) * 2 + 1];
+    }
+  }
+  __syncthreads();
+  if (warp != 0) return;
+
   int cur = 0, acc = 0, bonus = -1;
   if (lane == 0) a.path_nodes[static_cast<int64_t>(b) * (a.D + 1)] = 0;
 
   for (;;) {
     const int64_t row = nb + cur;
-    const ChunkStat *cs = a.stats + row * a.nch;
+    const ChunkStat *cs = (a.stage_stats ? s_cs : a.stats + nb * a.nch) + static_cast<int64_t>(cur) * a.nch;
     // row maximum (and, greedy, the argmax) from the chunk statistics
     float bm = -INFINITY;
     int ba = 0x7fffffff;
@@ -183,18 +213,18 @@ __global__ void __launch_bounds__(32) verify_walk_kernel(VerifyArgs a) {
       }
       Z = warp_sum(z);
       for (int base = 0; base < n && next < 0; base += 32) {
-        // the children among nodes base..base+31: each lane fetches its
-        // child's logit and uniform at once, then the decisions are taken
-        // in node order from registers
+        // the children among nodes base..base+31: each lane takes its
+        // child's logit and uniform, then the decisions are taken in node
+        // order from registers
         const int i = base + lane;
         const bool kid = i < n && s_par[i] == cur;
         int t_l = -1;
         float e_l = 0.f, u_l = 0.f;
         if (kid) {
           t_l = s_tok[i];
-          if (t_l >= 0 && t_l < a.V) e_l = ex2_approx(fmaf(logit_at<T>(a, row, t_l), sc, -mL));
+          if (t_l >= 0 && t_l < a.V) e_l = ex2_approx(fmaf(s_x[i], sc, -mL));
           else report(a.status, EAGLE_ERR_INVALID);
-          u_l = a.u[(nb + i) * 2 + 0];
+          u_l = s_u[2 * i];
         }
         unsigned bal = __ballot_sync(0xffffffffu, kid);
         while (bal && next < 0) {
@@ -220,7 +250,7 @@ __global__ void __launch_bounds__(32) verify_walk_kernel(VerifyArgs a) {
     if (next < 0 || acc >= a.D) {
       if (sample) {
         // ---- bonus: inverse CDF of the residual over the row -------------
-        const float target = a.u[(nb + cur) * 2 + 1] * (Z - rej_sum);
+        const float target = s_u[2 * cur + 1] * (Z - rej_sum);
         // chunk masses; lane l owns a contiguous block of chunks
         const int cpl = (a.nch + 31) / 32;
         const int c0 = lane * cpl, c1 = min(a.nch, c0 + cpl);
@@ -376,13 +406,14 @@ static cudaError_t launch_verify_t(const VerifyArgs &a, int num_sms, cudaStream_
                       : launch_chained(verify_stats_kernel<T, false>, dim3(static_cast<int>(blocks)), dim3(256), 0,
                                        st, a);
   if (e != cudaSuccess) return e;
-  const size_t smem = sizeof(int) * 4 * static_cast<size_t>(a.n);
+  size_t smem = sizeof(int) * 7 * static_cast<size_t>(a.n);
+  if (a.stage_stats) smem += sizeof(ChunkStat) * static_cast<size_t>(a.n) * a.nch;
   if (smem > 48 * 1024) {
     e = cudaFuncSetAttribute(verify_walk_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  return launch_chained(verify_walk_kernel<T>, dim3(a.B), dim3(32), smem, st, a);
+  return launch_chained(verify_walk_kernel<T>, dim3(a.B), dim3(kWalkThreads), smem, st, a);
 }
 
 cudaError_t launch_verify(const void *target, int dtype, int64_t ld, const int32_t *node_tok,
@@ -395,6 +426,10 @@ cudaError_t launch_verify(const void *target, int dtype, int64_t ld, const int32
   a.node_tok = node_tok; a.node_parent = node_parent;
   a.B = B; a.m = m; a.n = m + 1; a.D = D; a.V = V;
   a.nch = verify_chunks(V);
+  // the walk copies the chunk statistics of its sequence to shared memory
+  // when they fit beside its other arrays
+  a.stage_stats = sizeof(ChunkStat) * static_cast<size_t>(a.n) * a.nch + sizeof(int) * 7 * static_cast<size_t>(a.n) <=
+                  200 * 1024;
   a.mode = mode;
   a.inv_t = mode == EAGLE_SAMPLE ? 1.0f / temperature : 1.0f;
   a.u = u;
