@@ -10,8 +10,8 @@
 // One CTA per sequence, everything in shared memory.  A candidate is a
 // 64-bit key  bits(V):32 | (4095 - parent gid):12 | (2^20 - 1 - token):20,
 // so unsigned order is the rank order (V desc, parent gid asc, token asc)
-// and keys are unique.  Ranks are obtained by counting larger keys (4 lanes
-// per item, shuffle-reduced).  The running top-m list is merged with each
+// and keys are unique.  Ranks are obtained by counting larger keys (one
+// thread per item, the lanes of a warp reading the same keys).  The running top-m list is merged with each
 // new layer by rank arithmetic, so the whole candidate set is never sorted.
 //
 // Ablation variants ([EAGLE-2] section "実験結果", ablation table), chosen by
