@@ -272,6 +272,12 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
       }
       issued = j + 1;
     }
+    // an empty split's Q copy (no MMA waits for it) lands before the
+    // teardown barrier, so nothing written to the Q buffer after it races it
+    if (a.q_tma && T == 0 && lane == 0) {
+      volatile int never = 0;
+      mbar_wait(q_full, 0, &never, 100000000ull);
+    }
   } else if (warp == mma_warp) {
     // --------------------------------------------------------------------- MMA
     if (lane == 0) {
@@ -509,10 +515,6 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (a.q_tma && T == 0 && warp == producer_warp && lane == 0) {
-    volatile int never = 0;
-    mbar_wait(q_full, 0, &never, 100000000ull);  // nothing else waits for an empty split's Q copy
-  }
   if (*abort_flag) {
     if (tid == 0) report(a.status, EAGLE_ERR_TIMEOUT);
     volatile int never = 0;
