@@ -7,7 +7,8 @@ tolerances.
 
 Shapes cover both launch forms: one sequence of Llama-2-7B-shaped rows
 (few rows: 16-warp CTAs, each row split over a cluster of CTAs) and four
-sequences (8-warp CTAs), in bf16 and fp32, plus k = 32.
+sequences (8-warp CTAs), in bf16 and fp32, plus k = 32 (also with every
+row split over an 8-CTA cluster).
 """
 import numpy as np
 import pytest
@@ -54,6 +55,7 @@ CASES = [
     ("f32", 4, 6, 10, 32000),
     ("bf16", 1, 3, 32, 4096),
     ("bf16", 2, 2, 4, 201088),
+    ("bf16", 1, 2, 32, 201088),     # 8-part clusters with k = 32: the part merge ranks 256 keys
 ]
 
 
