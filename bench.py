@@ -36,6 +36,7 @@ if "--cpu-worker" in sys.argv or "reference" in sys.argv:
 MAIN_WORKLOAD = "llama2-7b-b1"      # B=1, Llama-2-7B-shaped
 ALSO_WORKLOAD = "gpt-oss-20b-b64"   # B=64, GPT-OSS-20B-shaped high concurrency
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+STAGE_LAUNCHES = 10   # launches per stage-timing graph
 
 
 def parse_args(argv=None):
@@ -243,7 +244,9 @@ def bench_workload(w, args, rank, world, device, with_e2e):
         step(**sets[i % copies])
     torch.cuda.synchronize()
 
-    # one graph per input copy for the whole step, one per stage
+    # one graph per input copy for the whole step; per stage, graphs of
+    # STAGE_LAUNCHES back-to-back launches over rotating input copies, so a
+    # stage's time per launch excludes the cost of submitting a graph
     graphs, stage_graphs = [], {k: [] for k in stages}
     for c in range(copies):
         g = torch.cuda.CUDAGraph()
@@ -253,7 +256,8 @@ def bench_workload(w, args, rank, world, device, with_e2e):
         for name, fn in stages.items():
             sg = torch.cuda.CUDAGraph()
             with torch.cuda.graph(sg):
-                fn(sets[c])
+                for i in range(STAGE_LAUNCHES):
+                    fn(sets[(c + i) % copies])
             stage_graphs[name].append(sg)
     torch.cuda.synchronize()
 
@@ -289,9 +293,10 @@ def bench_workload(w, args, rank, world, device, with_e2e):
         elapsed_ms = start.elapsed_time(stop)
     clocks = clk.summary()
 
-    # per stage: average duration of its launches, replayed back to back
+    # per stage: average duration of its launches (CUDA events on the
+    # launching stream around graphs of back-to-back launches)
     stage_ms = {}
-    reps = max(args.steps, 20)
+    reps = max(2, (max(args.steps, 20) + STAGE_LAUNCHES - 1) // STAGE_LAUNCHES)
     for name, gl in stage_graphs.items():
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -300,7 +305,7 @@ def bench_workload(w, args, rank, world, device, with_e2e):
             gl[r % copies].replay()
         b.record(stream)
         torch.cuda.synchronize()
-        stage_ms[name] = a.elapsed_time(b) / reps
+        stage_ms[name] = a.elapsed_time(b) / (reps * STAGE_LAUNCHES)
 
     elapsed_ms = max_over_ranks(elapsed_ms, device)   # the slowest replica sets the job's time
     ms_per_step = elapsed_ms / args.steps
