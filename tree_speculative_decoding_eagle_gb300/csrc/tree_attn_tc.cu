@@ -56,19 +56,32 @@ struct TcArgs {
   float scale_log2;  // softmax scale times log2(e)
   __nv_bfloat16 *out;
   float *lse;
-  int q_tma;          // 1: Q tiles arrive by TMA (128 % G == 0), else plain loads
+  int q_tma;          // 1: Q tiles arrive by TMA (G divides the region's rows), else plain loads
   int32_t *status;
 };
 
-template <int DH, int MT, int NK, int STAGES>
+// QR: query rows held per M-tile region.  128 normally; 64 when a group
+// has at most 64 rows (node, grouped head): the 128-row MMAs then read
+// rows 64-127 of each region from the neighbouring shared memory, and those
+// rows' results are never written out (rows are independent in S = Q K^T
+// and P.V), which frees shared memory for a third stage.
+template <int DH, int MT, int NK, int STAGES, int QR = 128>
 struct TcShape {
   static constexpr int kRegions = DH / 64;                   // 128-byte swizzle atoms per row
-  static constexpr int kQBytes = MT * kRegions * 16384;      // 128 rows x dh per M-tile
+  static constexpr int kQRegionBytes = QR * 128;             // QR rows x 64 columns
+  static constexpr int kQBytes = MT * kRegions * kQRegionBytes;
   static constexpr int kTileBytes = kRegions * NK * 128;     // one K (or V) tile
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kBarOff = kQBytes + STAGES * kStageBytes;
   static constexpr int kNumBars = 2 * STAGES + 4 * MT + 6;
-  static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;  // + alignment slack
+  static constexpr int kBarBytes = kNumBars * 8 + 16;
+  // QR = 128: buffers at the first 1 KB boundary, barriers after them.
+  // QR = 64: the barriers sit in the gap before the 1 KB-aligned buffers
+  // when it holds them, else after the buffers; with a 16-byte aligned base
+  // either way ends within kBarOff + max(1008, 2 kBarBytes - 16) bytes.
+  static constexpr int kSmem = QR == 128 ? kBarOff + kBarBytes + 1024
+                                         : kBarOff + (1008 > 2 * kBarBytes - 16 ? 1008 : 2 * kBarBytes - 16);
+  static_assert(QR == 128 || (QR == 64 && MT == 1), "64-row regions with one M-tile only");
   static constexpr int kThreads = MT * 128 + 64;
   static constexpr int kColS = 0;                            // S_t at t*NK
   static constexpr int kColP = MT * NK;                      // P_t at kColP + t*NK/2
@@ -86,19 +99,26 @@ constexpr int kMaxClusterSplits = 8;
 
 // SPLIT: the grid splits the KV range (S > 1) and the kernel carries the
 // cluster merge; without it the merge code is compiled out.
-template <int DH, int MT, int NK, int STAGES, bool SPLIT>
+template <int DH, int MT, int NK, int STAGES, bool SPLIT, int QR>
 __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
     tree_attn_tc_kernel(const __grid_constant__ CUtensorMap kc_map, const __grid_constant__ CUtensorMap vc_map,
                         const __grid_constant__ CUtensorMap kt_map, const __grid_constant__ CUtensorMap vt_map,
                         const __grid_constant__ CUtensorMap q_map, TcArgs a) {
-  using Sh = TcShape<DH, MT, NK, STAGES>;
+  using Sh = TcShape<DH, MT, NK, STAGES, QR>;
   constexpr int NH = NK / 64;  // 64-key halves of a tile
   extern __shared__ unsigned char raw_smem[];
-  unsigned char *sm = reinterpret_cast<unsigned char *>(
-      (reinterpret_cast<uintptr_t>(raw_smem) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uintptr_t raw = reinterpret_cast<uintptr_t>(raw_smem);
+  unsigned char *sm = reinterpret_cast<unsigned char *>((raw + 1023) & ~static_cast<uintptr_t>(1023));
   unsigned char *sQ = sm;
   unsigned char *sKV = sm + Sh::kQBytes;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + Sh::kBarOff);
+  uint64_t *bars;
+  if constexpr (QR == 128) {
+    bars = reinterpret_cast<uint64_t *>(sm + Sh::kBarOff);
+  } else {
+    bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uintptr_t>(sm) - raw >= static_cast<uintptr_t>(Sh::kBarBytes)
+                                            ? raw_smem
+                                            : sm + Sh::kBarOff);
+  }
   uint64_t *kv_full = bars;
   uint64_t *kv_empty = bars + STAGES;
   uint64_t *s_full = bars + 2 * STAGES;
@@ -134,9 +154,9 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
   // sequence's last node hold the next sequence's queries (their outputs
   // are never written).  Otherwise plain loads with zero rows.
   const int rows_total = n * a.G;
-  for (int idx = tid; !a.q_tma && idx < MT * 128 * (DH / 8); idx += Sh::kThreads) {
-    const int t = idx / (128 * (DH / 8));
-    const int rem = idx % (128 * (DH / 8));
+  for (int idx = tid; !a.q_tma && idx < MT * QR * (DH / 8); idx += Sh::kThreads) {
+    const int t = idx / (QR * (DH / 8));
+    const int rem = idx % (QR * (DH / 8));
     const int r = rem / (DH / 8), c = rem % (DH / 8);
     const int rho = (mg * MT + t) * 128 + r;
     uint4 v = make_uint4(0, 0, 0, 0);
@@ -145,7 +165,7 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
       const __nv_bfloat16 *src = a.q + ((static_cast<int64_t>(b) * n + i) * a.Hq + g * a.G + hh) * DH;
       v = *reinterpret_cast<const uint4 *>(src + c * 8);
     }
-    *reinterpret_cast<uint4 *>(sQ + (t * Sh::kRegions + c / 8) * 16384 + sw128_offset(r, c % 8)) = v;
+    *reinterpret_cast<uint4 *>(sQ + (t * Sh::kRegions + c / 8) * Sh::kQRegionBytes + sw128_offset(r, c % 8)) = v;
   }
   fence_async_smem();
   if (tid == 0) {
@@ -189,11 +209,11 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
       if (a.q_tma) {
-        mbar_arrive_expect_tx(q_full, MT * Sh::kRegions * 16384);
+        mbar_arrive_expect_tx(q_full, MT * Sh::kRegions * Sh::kQRegionBytes);
         for (int t = 0; t < MT; ++t)
 #pragma unroll
           for (int r = 0; r < Sh::kRegions; ++r)
-            tma_load_3d(sQ + (t * Sh::kRegions + r) * 16384, &q_map, r * 64, g * a.G,
+            tma_load_3d(sQ + (t * Sh::kRegions + r) * Sh::kQRegionBytes, &q_map, r * 64, g * a.G,
                         b * n + (mg * MT + t) * (128 / a.G), q_full);
       }
       prefetch_tmap(&kc_map);
@@ -285,10 +305,10 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
       constexpr uint32_t id_o = idesc_bf16(128, DH, true);
       auto issue_s = [&](int j, int t) {
         const uint32_t kaddr = smem_u32(sKV + (j % STAGES) * Sh::kStageBytes);
-        const uint32_t qaddr = smem_u32(sQ + t * Sh::kRegions * 16384);
+        const uint32_t qaddr = smem_u32(sQ + t * Sh::kRegions * Sh::kQRegionBytes);
 #pragma unroll
         for (int s = 0; s < DH / 16; ++s) {
-          const uint64_t ad = sdesc_sw128(qaddr + (s / 4) * 16384 + (s % 4) * 32, 16, 1024);
+          const uint64_t ad = sdesc_sw128(qaddr + (s / 4) * Sh::kQRegionBytes + (s % 4) * 32, 16, 1024);
           const uint64_t bd = sdesc_sw128(kaddr + (s / 4) * (NK * 128) + (s % 4) * 32, 16, 1024);
           mma_bf16_ss(tmem + Sh::kColS + t * NK, ad, bd, id_s, s > 0);
         }
@@ -689,13 +709,13 @@ static bool make_kv_map(CUtensorMap *map, const void *base, int64_t rows, int dh
 }
 
 // Q [B*n, Hq, dh] bf16 viewed as a 3D tensor with boxes of 64 columns x G
-// heads x 128/G nodes (128-byte swizzle): one box is one M-tile region.
-static bool make_q_map(CUtensorMap *map, const void *base, int64_t rows, int Hq, int dh, int G) {
+// heads x box_rows/G nodes (128-byte swizzle): one box is one M-tile region.
+static bool make_q_map(CUtensorMap *map, const void *base, int64_t rows, int Hq, int dh, int G, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(dh), static_cast<cuuint64_t>(Hq), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(dh) * 2, static_cast<cuuint64_t>(Hq) * dh * 2};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(128 / G)};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(box_rows / G)};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -739,29 +759,29 @@ static TcPlan tc_plan(int B, int n, int Hq, int Hkv, int dh, int Lmax, int num_s
 // The splits merge through distributed shared memory: no workspace.
 size_t attn_tc_workspace_bytes(int, int, int, int, int, int, int) { return 0; }
 
-template <int DH, int MT, int NK, int STAGES, bool SPLIT>
+template <int DH, int MT, int NK, int STAGES, bool SPLIT, int QR>
 static cudaError_t launch_tc_v(const CUtensorMap *maps, const TcArgs &a, const TcPlan &p, cudaStream_t st) {
-  using Sh = TcShape<DH, MT, NK, STAGES>;
+  using Sh = TcShape<DH, MT, NK, STAGES, QR>;
   static_assert(Sh::kSmem <= 232448, "shared memory budget");
   // MT = 1 variants run two CTAs per SM (228 KB per SM, 1 KB reserved per CTA)
   static_assert(MT != 1 || 2 * (Sh::kSmem + 1024) <= 233472, "two CTAs per SM");
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(tree_attn_tc_kernel<DH, MT, NK, STAGES, SPLIT>,
+    cudaError_t e = cudaFuncSetAttribute(tree_attn_tc_kernel<DH, MT, NK, STAGES, SPLIT, QR>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   // the S splits of one (b, g, M-group) form one cluster
   dim3 grid(p.S, p.mgroups, a.B * a.Hkv);
-  return launch_chained_cluster(tree_attn_tc_kernel<DH, MT, NK, STAGES, SPLIT>, grid, dim3(Sh::kThreads), Sh::kSmem,
+  return launch_chained_cluster(tree_attn_tc_kernel<DH, MT, NK, STAGES, SPLIT, QR>, grid, dim3(Sh::kThreads), Sh::kSmem,
                                 st, p.S, maps[0], maps[1], maps[2], maps[3], maps[4], a);
 }
 
-template <int DH, int MT, int NK, int STAGES>
+template <int DH, int MT, int NK, int STAGES, int QR = 128>
 static cudaError_t launch_tc_t(const CUtensorMap *maps, const TcArgs &a, const TcPlan &p, cudaStream_t st) {
-  return p.S > 1 ? launch_tc_v<DH, MT, NK, STAGES, true>(maps, a, p, st)
-                 : launch_tc_v<DH, MT, NK, STAGES, false>(maps, a, p, st);
+  return p.S > 1 ? launch_tc_v<DH, MT, NK, STAGES, true, QR>(maps, a, p, st)
+                 : launch_tc_v<DH, MT, NK, STAGES, false, QR>(maps, a, p, st);
 }
 
 // Common launcher; block_table == nullptr is the contiguous cache, otherwise
@@ -782,7 +802,11 @@ static cudaError_t launch_tc_common(const void *q, const void *k_cache, const vo
       !make_kv_map(&maps[2], k_tree, tree_rows, dh, p.NK) || !make_kv_map(&maps[3], v_tree, tree_rows, dh, p.NK))
     return cudaErrorInvalidValue;
   const int G = Hq / Hkv;
-  const bool q_tma = 128 % G == 0 && make_q_map(&maps[4], q, static_cast<int64_t>(B) * n, Hq, dh, G);
+  // at most 64 rows (node, grouped head) per group and dh = 128: 64-row Q
+  // regions and a third stage
+  const bool half_q = dh == 128 && n * G <= 64;
+  const int q_rows = half_q ? 64 : 128;
+  const bool q_tma = q_rows % G == 0 && make_q_map(&maps[4], q, static_cast<int64_t>(B) * n, Hq, dh, G, q_rows);
   if (!q_tma) maps[4] = maps[2];  // unused
   TcArgs a;
   a.q = reinterpret_cast<const __nv_bfloat16 *>(q);
@@ -803,6 +827,8 @@ static cudaError_t launch_tc_common(const void *q, const void *k_cache, const vo
   // stages: as many as shared memory allows at the variant's CTAs per SM
   if (dh == 64) {
     e = p.MT == 1 ? launch_tc_t<64, 1, 128, 2>(maps, a, p, st) : launch_tc_t<64, 2, 128, 4>(maps, a, p, st);
+  } else if (half_q) {
+    e = launch_tc_t<128, 1, 64, 3, 64>(maps, a, p, st);
   } else {
     e = p.MT == 1 ? launch_tc_t<128, 1, 64, 2>(maps, a, p, st) : launch_tc_t<128, 2, 64, 4>(maps, a, p, st);
   }
