@@ -108,29 +108,6 @@ template <> __device__ __forceinline__ float vec_max<__nv_bfloat16>(const uint4 
   return fmaxf(bf16_lo(w), bf16_hi(w));
 }
 
-// Sum over a 16-byte vector of 2^(x*log2e - mL), as a packed pair of partial
-// sums accumulated into acc.
-template <typename T> __device__ __forceinline__ uint64_t vec_exp_sum(const uint4 &v, uint64_t L2, uint64_t nmL2, uint64_t acc);
-template <> __device__ __forceinline__ uint64_t vec_exp_sum<__nv_bfloat16>(const uint4 &v, uint64_t L2, uint64_t nmL2,
-                                                                           uint64_t acc) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    float t0, t1;
-    f2_unpack(f2_fma(f2_pack(bf16_lo(w[q]), bf16_hi(w[q])), L2, nmL2), t0, t1);
-    acc = f2_add(acc, f2_pack(ex2_approx(t0), ex2_approx(t1)));
-  }
-  return acc;
-}
-template <> __device__ __forceinline__ uint64_t vec_exp_sum<float>(const uint4 &v, uint64_t L2, uint64_t nmL2,
-                                                                   uint64_t acc) {
-  float t0, t1;
-  f2_unpack(f2_fma(f2_pack(__uint_as_float(v.x), __uint_as_float(v.y)), L2, nmL2), t0, t1);
-  acc = f2_add(acc, f2_pack(ex2_approx(t0), ex2_approx(t1)));
-  f2_unpack(f2_fma(f2_pack(__uint_as_float(v.z), __uint_as_float(v.w)), L2, nmL2), t0, t1);
-  return f2_add(acc, f2_pack(ex2_approx(t0), ex2_approx(t1)));
-}
-
 // Streaming 16-byte load that does not allocate in L1.
 __device__ __forceinline__ uint4 ld_stream16(const void *p) {
   uint4 v;
@@ -169,53 +146,6 @@ __device__ __forceinline__ void lse_combine(float &m, float &s, float m2, float 
   if (mn == -INFINITY) return;  // both empty
   s = s * ex2_approx((m - mn) * kLog2e) + s2 * ex2_approx((m2 - mn) * kLog2e);
   m = mn;
-}
-
-// ---- sorted top-K lists of unique 64-bit keys (descending) ---------------
-// Insert `key` into a register list kept in descending order (keys unique).
-template <int K>
-__device__ __forceinline__ void list_insert(uint64_t (&list)[K], uint64_t key) {
-#pragma unroll
-  for (int j = 0; j < K; ++j) {
-    uint64_t a = list[j];
-    bool gt = key > a;
-    list[j] = gt ? key : a;
-    key = gt ? a : key;
-  }
-}
-
-// Bitonic merge: keep the K largest of two descending lists A (registers)
-// and B (partner lane's list via shuffles), result descending in A.
-template <int K>
-__device__ __forceinline__ void list_merge_xor(uint64_t (&a)[K], int lane_xor) {
-  uint64_t b[K];
-#pragma unroll
-  for (int j = 0; j < K; ++j) b[j] = shfl_xor_u64(a[j], lane_xor);
-  // a[j] vs b[K-1-j]: elementwise max gives the top K as a bitonic sequence
-#pragma unroll
-  for (int j = 0; j < K; ++j) {
-    uint64_t o = b[K - 1 - j];
-    a[j] = a[j] > o ? a[j] : o;
-  }
-  // bitonic sort descending
-#pragma unroll
-  for (int s = K / 2; s > 0; s >>= 1) {
-#pragma unroll
-    for (int j = 0; j < K; ++j) {
-      if ((j & s) == 0) {
-        uint64_t x = a[j], y = a[j + s];
-        a[j] = x > y ? x : y;
-        a[j + s] = x > y ? y : x;
-      }
-    }
-  }
-}
-
-// Warp-wide top-K: after this every lane holds the warp's K largest keys.
-template <int K>
-__device__ __forceinline__ void warp_topk(uint64_t (&a)[K]) {
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) list_merge_xor<K>(a, o);
 }
 
 // ---- chained launches (programmatic dependent launch) --------------------
