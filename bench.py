@@ -51,6 +51,8 @@ def parse_args(argv=None):
     p.add_argument("--impl", default="ours", choices=("ours", "reference"))
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-next-rows", action="store_true",
+                   help="skip the per-launch times of the paged, commit, draft-verify, static-tree and ablation rows")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     p.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
     return p.parse_args(argv)
@@ -217,7 +219,108 @@ def build_inputs(w, device):
     return step, inputs, ai["kv_len"].cpu().numpy(), depth_sum
 
 
-def bench_workload(w, args, rank, world, device, with_e2e):
+def measure_next_rows(step, sets, w, work, peaks):
+    """Per-launch times of the rows built after the step's own (paged-prefix
+    attention, KV commit, verification against the draft distribution, the
+    static tree, the two ablation variants of the tree build) on this
+    workload's inputs: CUDA events around graphs of STAGE_LAUNCHES
+    back-to-back launches (the KV commit's graph also resets kv_len once)."""
+    import numpy as np
+    import torch
+    import gen
+    import tree_speculative_decoding_eagle_gb300 as eg
+    stream = torch.cuda.current_stream()
+    copies = len(sets)
+
+    def per_launch_ms(fn, reps=4):
+        for i in range(3):
+            fn(i)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(STAGE_LAUNCHES):
+                fn(i)
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / (reps * STAGE_LAUNCHES)
+
+    out = {"workload": w.name}
+    T = step.tree
+    # f1: attention over a paged prefix (the same caches scattered into page
+    # pools through a shuffled block table), and the KV commit
+    B, Hkv, Lmax, dh = sets[0]["k_cache"].shape
+    paged = {}
+    for P in (16, 64):
+        if Lmax % P:
+            continue
+        mp = Lmax // P
+        num_pages = B * mp + 8
+        table = torch.randperm(num_pages, device=sets[0]["q"].device)[:B * mp].view(B, mp).to(torch.int32)
+        pools = []
+        for c in range(copies):
+            pk = torch.zeros((num_pages, Hkv, P, dh), dtype=sets[c]["k_cache"].dtype, device=table.device)
+            pv = torch.zeros_like(pk)
+            idx = table.reshape(-1).long()
+            pk[idx] = sets[c]["k_cache"].view(B, Hkv, mp, P, dh).permute(0, 2, 1, 3, 4).reshape(B * mp, Hkv, P, dh)
+            pv[idx] = sets[c]["v_cache"].view(B, Hkv, mp, P, dh).permute(0, 2, 1, 3, 4).reshape(B * mp, Hkv, P, dh)
+            pools.append((pk, pv))
+        o = torch.empty_like(sets[0]["q"])
+        lse = torch.empty(step.lse.shape, dtype=torch.float32, device=table.device)
+        ws = eg.Workspace(table.device)
+
+        def run(i, P=P, pools=pools, table=table, o=o, lse=lse, ws=ws):
+            s_ = sets[i % copies]
+            pk, pv = pools[i % copies]
+            eg.tree_attn_paged(s_["q"], pk, pv, table, s_["kv_len"], s_["k_tree"], s_["v_tree"], T["mask"],
+                               out=o, lse=lse, workspace=ws)
+        ms = per_launch_ms(run)
+        gbs = work["tree_attn"] / (ms * 1e-3) / 1e9
+        paged[f"page_{P}"] = {"ms": round(ms, 5), "gbs": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm_gbs"], 4)}
+        del pools
+    out["paged_attention"] = paged
+    # the KV commit of the last step's accepted path into the contiguous
+    # cache: a graph of STAGE_LAUNCHES commits from a length that leaves room
+    # for all of them, kv_len reset once per graph (one 4-byte copy)
+    s0 = sets[0]
+    base_kvl = torch.full_like(s0["kv_len"], Lmax - STAGE_LAUNCHES * w.D - 1)
+    kvl = base_kvl.clone()
+    status = torch.zeros(1, dtype=torch.int32, device=kvl.device)
+
+    def run_commit(i):
+        if i % STAGE_LAUNCHES == 0:
+            kvl.copy_(base_kvl)
+        eg.kv_commit(s0["k_tree"], s0["v_tree"], step.accept_len, step.path_nodes, s0["k_cache"], s0["v_cache"],
+                     kvl, status=status)
+    out["kv_commit"] = {"ms": round(per_launch_ms(run_commit), 5), "accepted": int(step.accept_len.sum().item())}
+    out["kv_commit"]["status"] = int(status.item())
+    # f2: speculative-sampling verification against the draft distributions
+    n = w.m + 1
+    u = torch.rand((w.B, n, 2), device=kvl.device)
+
+    def run_vd(i):
+        s_ = sets[i % copies]
+        eg.verify_draft(s_["target"], s_["draft_logits"], T["tok"], T["parent"], T["row"], w.D, w.temperature, u)
+    out["verify_draft"] = {"ms": round(per_launch_ms(run_vd), 5)}
+    # f3: the EAGLE-1 static tree from a fixed template
+    tp, tr = gen.static_template()
+    tpar = torch.from_numpy(tp).to(kvl.device)
+    trank = torch.from_numpy(tr).to(kvl.device)
+    out["static_tree"] = {"ms": round(per_launch_ms(lambda i: eg.static_tree(step.tok, step.conf, tpar, trank)), 5),
+                          "nodes": int(tp.shape[0])}
+    # f4: the ablation variants of the tree build, beside the method itself
+    for name, flags in (("tree_build", 0), ("tree_build_confidence_only", eg.TREE_CONFIDENCE_ONLY),
+                        ("tree_build_no_rerank", eg.TREE_NO_RERANK)):
+        out[name] = {"ms": round(per_launch_ms(lambda i, f=flags: eg.tree_build(step.tok, step.conf, w.m, flags=f)), 5)}
+    return out
+
+
+def bench_workload(w, args, rank, world, device, with_e2e, next_rows=False):
     import torch
     from tree_speculative_decoding_eagle_gb300.replicas import max_over_ranks
 
@@ -314,11 +417,12 @@ def bench_workload(w, args, rank, world, device, with_e2e):
     e2e = None
     if with_e2e:
         e2e = bench_e2e(step, base, graphs[0], sets[0], args, world, device)
+    nxt = measure_next_rows(step, sets, w, work, load_peaks()[0]) if next_rows and rank == 0 else None
 
     tau = float(step.accept_len.float().mean().item())
     return dict(w=w, work=work, ms_per_step=ms_per_step, value=value, clocks=clocks,
                 stage_ms=stage_ms, copies=copies, e2e=e2e, tau=tau, step_bytes=step_bytes,
-                l2=l2)
+                l2=l2, next_rows=nxt)
 
 
 def bench_e2e(step, base, graph, dev_set, args, world, device):
@@ -525,7 +629,7 @@ def main(argv=None):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = run_cpu_baseline(args.workload, args.cpu_seconds)
-    res = bench_workload(w, args, rank, world, device, with_e2e=not args.no_e2e)
+    res = bench_workload(w, args, rank, world, device, with_e2e=not args.no_e2e, next_rows=not args.no_next_rows)
     also = None
     if args.also and args.also != "none" and args.also != args.workload:
         w2 = gen.WORKLOADS[args.also]
@@ -565,6 +669,7 @@ def main(argv=None):
         "clocks": res["clocks"],
         "mean_accept_len": res["tau"],
         "also": also,
+        "next_rows": res["next_rows"],
     }
     print(json.dumps(line), flush=True)
     if world > 1:
