@@ -149,8 +149,12 @@ int eagle_draft_topk_noalloc(const void *logits, int dtype, int B, int D, int k,
  *                expanded with row [d, j], root 0, else -1; may be NULL)
  *   mask         device uint64 [B, m+1, W], W = ceil((m+1)/64) (out; may be
  *                NULL) — the same words eagle_tree_mask writes
- *   status       device int32 (out; may be NULL): EAGLE_ERR_INVALID when an
- *                input is outside the domain above
+ *   status       device int32 (out; may be NULL): EAGLE_ERR_INVALID when a
+ *                token or confidence is outside its range above.  Repeated
+ *                tokens within a row are not checked (stage 1 never writes
+ *                them): the tree is then unspecified, but every output
+ *                index stays in range and nothing is read or written out of
+ *                bounds.
  * Limits: 1 <= k <= 32, D >= 1, 1 <= m <= k + (D-1)k^2 <= 4095.
  * ------------------------------------------------------------------------ */
 int eagle_tree_build(const int32_t *tok, const float *conf, int B, int D, int k,

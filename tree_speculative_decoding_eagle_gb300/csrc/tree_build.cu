@@ -111,23 +111,36 @@ __global__ void __launch_bounds__(kTreeThreads) tree_build_kernel(TreeArgs a) {
   const float *conf = a.conf + static_cast<int64_t>(b) * D * kk;
 
   pdl_wait();
-  if (tid == 0) s_bad = 0;
+  if (tid == 0) {
+    s_bad = 0;
+    s_key[0] = tree_key(1.0f, 0, 0);  // the root: V = 1, parent field decodes to gid 0
+  }
   for (int g = tid; g <= NC; g += blockDim.x) {
     s_row[g] = g == 0 ? 0 : -1;
     s_out[g] = g == 0 ? 0 : -1;
   }
-  // used draft rows (slot 0 = row [0,0], slot 1+(d-1)k+j = row [d,j]) in one
-  // coalesced pass; tokens and confidences outside the domain are flagged and
-  // tokens clamped so the key fields stay in range
+  // every gid slot starts valid, so colliding ranks (only from a row that
+  // repeats a token, outside the domain) never index out of range
+  for (int q = tid; q < 2 * m || q < k; q += blockDim.x) {
+    if (q < 2 * m) {
+      s_L[q] = 0;
+      s_Lg[q] = 0;
+    }
+    if (q < m) s_sel[q] = 0;
+    if (q < k) s_E[q] = 0;
+  }
+  // used draft rows, row [0,0] then rows [1..D-1, *]: contiguous in the
+  // input after its first k values (slot 0 = row [0,0], slot 1+(d-1)k+j =
+  // row [d,j]), read in one coalesced pass; tokens and confidences outside
+  // the domain are flagged and tokens clamped so the key fields stay in range
   for (int idx = tid; idx < R * k; idx += blockDim.x) {
-    const int slot = idx / k, rr = idx % k;
-    const int gi = slot == 0 ? rr : ((1 + (slot - 1) / k) * k + (slot - 1) % k) * k + rr;
+    const int gi = idx < k ? idx : kk + (idx - k);
     int t = tok[gi];
     const float c = conf[gi];
     if (!(c >= 0.f && c <= 1.f) || t < 0 || t > 0xFFFFF) s_bad = 1;
     if (t < 0 || t > 0xFFFFF) t = 0;
     s_tok[idx] = t;
-    s_conf[idx] = c;
+    s_conf[idx] = __fadd_rn(c, 0.0f);  // -0 -> +0: the key's unsigned order is then the float order
   }
   __syncthreads();
 
@@ -198,7 +211,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_build_kernel(TreeArgs a) {
       const int nbase = layer_base(d + 1, k);
       for (int q = tid; q < kk; q += blockDim.x) {
         const int j = q / k, r = q % k;
-        const int p = s_E[j];
+        const int p = min(max(s_E[j], 0), NC);
         const int slot = (1 + (d - 1) * k + j) * k + r;
         const float cf = s_conf[slot];
         const float v = conf_only ? cf : __fadd_rn(__fmul_rn(tkey_score(s_key[p]), cf), 0.0f);
@@ -266,7 +279,11 @@ __global__ void __launch_bounds__(kTreeThreads) tree_build_kernel(TreeArgs a) {
       __syncthreads();
     }
   } else {
-    for (int q = tid; q < m; q += blockDim.x) s_out[sel[q]] = q + 1;
+    for (int q = tid; q < m; q += blockDim.x) {
+      const int g = sel[q];
+      if (g > 0 && g <= NC) s_out[g] = q + 1;
+      else s_bad = 1;
+    }
   }
   __syncthreads();
 
@@ -279,7 +296,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_build_kernel(TreeArgs a) {
   const int W = (n + 63) >> 6;
   for (int q = tid; q < n * W; q += blockDim.x) {
     const int i = q / W, w = q % W;
-    const int src = i == 0 ? 0 : sel[i - 1];
+    const int src = i == 0 ? 0 : min(max(sel[i - 1], 0), NC);
     if (w == 0) {
       int t, par, dep, row;
       float sc;
@@ -290,8 +307,9 @@ __global__ void __launch_bounds__(kTreeThreads) tree_build_kernel(TreeArgs a) {
         const uint64_t key = s_key[src];
         t = tkey_token(key);
         sc = tkey_score(key);
-        par = s_out[tkey_parent(key)];
-        if (par < 0 || par >= i) s_bad = 1;  // not closed: a confidence outside [0, 1]
+        const int pg = tkey_parent(key);
+        par = pg >= 0 && pg <= NC ? s_out[pg] : -1;
+        if (par < 0 || par >= i) s_bad = 1;  // not closed: an input outside the domain
         dep = depth_of_gid(src, k);
         row = s_row[src];
       }
