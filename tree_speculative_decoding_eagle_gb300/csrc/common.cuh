@@ -116,6 +116,19 @@ __device__ __forceinline__ uint4 ld_stream16(const void *p) {
   return v;
 }
 
+// Asynchronous 16-byte copy global -> shared (L2 only), committed in groups;
+// a thread waits for its own groups, so a lane that reads back only what it
+// copied needs no barrier.
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+               ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))), "l"(gmem_src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N> __device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // ---- warp reductions ------------------------------------------------------
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll

@@ -8,11 +8,13 @@
 // One pass over HBM.  A row is split into S <= 8 parts, one CTA each; the
 // parts of a row form one thread-block cluster.  Few rows (each part fits
 // one segment per warp with the parts of all rows resident at once) take
-// 16-warp CTAs with 1024-token segments; many rows take 8-warp CTAs with
-// 2048-token segments, three per SM.  Each warp holds a segment in
-// registers (all 16-byte loads in flight at once) and visits it twice: lane
-// maxima, then the sum of exp(x - segment max), folded into a running
-// (max, sum).  Top-k selection works on unique 64-bit keys (logit order,
+// 16-warp CTAs with 1024-token segments, held in registers (all 16-byte
+// loads in flight at once); many rows take 8-warp CTAs, three per SM, whose
+// warps stream 1024-token segments through a three-stage ring in shared
+// memory (asynchronous copies issued two segments ahead, so the loads stay
+// in flight while a segment is being processed).  A warp visits each
+// segment twice: lane maxima, then the sum of exp(x - segment max), folded
+// into a running (max, sum).  Top-k selection works on unique 64-bit keys (logit order,
 // then lower token id).  Each warp keeps its k best keys so far sorted in
 // registers (lane i holds the i-th); a new key's place is the number of
 // larger keys (one ballot) and the tail shifts down one lane.  The list's
@@ -99,6 +101,32 @@ template <> __device__ __forceinline__ float elem_of<float>(const uint4 &v, int 
   return __uint_as_float(e == 0 ? v.x : (e == 1 ? v.y : (e == 2 ? v.z : v.w)));
 }
 
+// Sum over a lane's vectors of 2^(x log2e + nmL): even and odd elements in
+// the two halves of a packed pair, one FMA and one add for every two
+// elements (each half rounds exactly as its scalar form).
+template <typename T, int NVL>
+__device__ __forceinline__ float segment_exp_sum(const uint4 (&vb)[NVL], int nvec, int lane, float nmL) {
+  constexpr int VEC = VecTraits<T>::kElems;
+  const uint64_t c2 = f2_pack(kLog2e, kLog2e), n2 = f2_pack(nmL, nmL);
+  uint64_t acc = f2_pack(0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < NVL; ++i) {
+    if (lane + 32 * i < nvec) {
+      float x[VEC];
+      VecTraits<T>::unpack(vb[i], x);
+#pragma unroll
+      for (int e = 0; e < VEC; e += 2) {
+        float y0, y1;
+        f2_unpack(f2_fma(f2_pack(x[e], x[e + 1]), c2, n2), y0, y1);
+        acc = f2_add(acc, f2_pack(ex2_approx(y0), ex2_approx(y1)));
+      }
+    }
+  }
+  float a0, a1;
+  f2_unpack(acc, a0, a1);
+  return a0 + a1;
+}
+
 // NW warps per CTA, NVL 16-byte vectors per lane and segment.
 template <typename T, int NW, int NVL>
 __global__ void __launch_bounds__(NW * 32, NW <= 8 ? 3 : 1) draft_topk_kernel(DraftArgs a) {
@@ -138,6 +166,26 @@ __global__ void __launch_bounds__(NW * 32, NW <= 8 ? 3 : 1) draft_topk_kernel(Dr
   const int spp = (nseg + a.S - 1) / a.S;
   const int g0 = part * spp, g1 = min(nseg, g0 + spp);
   uint4 vb[NVL];
+  // ring form (8-warp CTAs): warp w's stages at s_ring[(w * kStages + s) *
+  // NVL * 32], lane l's vectors l, l+32, ... of a segment in each; every
+  // iteration commits one copy group (empty past the part's end)
+  constexpr bool kRing = NW == 8;
+  constexpr int kStages = 3;
+  extern __shared__ __align__(16) uint4 s_ring[];
+  uint4 *my_ring = s_ring + warp * kStages * NVL * 32;
+  auto issue_segment = [&](int gseg, int stage) {
+    if (gseg < g1) {
+      const int seg0 = gseg * SEG;
+      const int nvec = min(SEG, a.V - seg0) / VEC;
+      uint4 *dst = my_ring + stage * NVL * 32;
+#pragma unroll
+      for (int i = 0; i < NVL; ++i) {
+        const int v = lane + 32 * i;
+        if (v < nvec) cp_async16(dst + v, row + seg0 + v * VEC);
+      }
+    }
+    cp_async_commit();
+  };
   auto load_segment = [&](int gseg) {
     const int seg0 = gseg * SEG;
     const int nvec = min(SEG, a.V - seg0) / VEC;
@@ -148,7 +196,13 @@ __global__ void __launch_bounds__(NW * 32, NW <= 8 ? 3 : 1) draft_topk_kernel(Dr
     }
   };
   pdl_wait();
-  if (g0 + warp < g1) load_segment(g0 + warp);  // in flight while the shared state is set up
+  // in flight while the shared state is set up
+  if constexpr (kRing) {
+#pragma unroll
+    for (int st = 0; st < kStages - 1; ++st) issue_segment(g0 + warp + st * NW, st);
+  } else {
+    if (g0 + warp < g1) load_segment(g0 + warp);
+  }
   if (tid == 0) {
     s_thr = ordered_u32(-INFINITY);
     s_nc = 0;
@@ -209,22 +263,8 @@ __global__ void __launch_bounds__(NW * 32, NW <= 8 ? 3 : 1) draft_topk_kernel(Dr
       if (lane == 0 && kth > -INFINITY) atomicMax(&s_thr, ordered_u32(kth));
     }
     if (smax > -INFINITY) {
-      const float nmL = -smax * kLog2e;
-      float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-      for (int i = 0; i < NVL; ++i) {
-        if (lane + 32 * i < nvec) {
-          float x[VEC];
-          VT::unpack(vb[i], x);
-#pragma unroll
-          for (int e = 0; e < VEC; e += 2) {
-            acc0 += ex2_approx(fmaf(x[e], kLog2e, nmL));
-            acc1 += ex2_approx(fmaf(x[e + 1], kLog2e, nmL));
-          }
-        }
-      }
       m = smax;
-      sum = acc0 + acc1;
+      sum = segment_exp_sum<T, NVL>(vb, nvec, lane, -smax * kLog2e);
     }
     pdl_trigger();
     {
@@ -313,10 +353,21 @@ __global__ void __launch_bounds__(NW * 32, NW <= 8 ? 3 : 1) draft_topk_kernel(Dr
     }
     __syncthreads();
   } else {
-    for (int gseg = g0 + warp; gseg < g1; gseg += NW) {
-      if (gseg != g0 + warp) load_segment(gseg);
+    for (int gseg = g0 + warp, it = 0; gseg < g1; gseg += NW, ++it) {
       const int seg0 = gseg * SEG;
       const int nvec = min(SEG, a.V - seg0) / VEC;
+      if constexpr (kRing) {
+        // the stage read one iteration ago takes the segment kStages-1 ahead;
+        // this iteration's copies are then complete
+        issue_segment(gseg + (kStages - 1) * NW, (it + kStages - 1) % kStages);
+        cp_async_wait<kStages - 1>();
+        const uint4 *src = my_ring + (it % kStages) * NVL * 32;
+#pragma unroll
+        for (int i = 0; i < NVL; ++i)
+          if (lane + 32 * i < nvec) vb[i] = src[lane + 32 * i];
+      } else {
+        if (gseg != g0 + warp) load_segment(gseg);
+      }
       float smax = -INFINITY;
       float vmx[NVL];
   #pragma unroll
@@ -324,33 +375,18 @@ __global__ void __launch_bounds__(NW * 32, NW <= 8 ? 3 : 1) draft_topk_kernel(Dr
         vmx[i] = (lane + 32 * i < nvec) ? vec_max<T>(vb[i]) : -INFINITY;
         smax = fmaxf(smax, vmx[i]);
       }
-      if (smax > -INFINITY) {
-        // sum of 2^(x*log2e - smax*log2e): per element one extract, FMA, ex2, add
-        const float nmL = -smax * kLog2e;
-        float acc0 = 0.f, acc1 = 0.f;
-  #pragma unroll
-        for (int i = 0; i < NVL; ++i) {
-          if (lane + 32 * i < nvec) {
-            float x[VEC];
-            VT::unpack(vb[i], x);
-  #pragma unroll
-            for (int e = 0; e < VEC; e += 2) {
-              acc0 += ex2_approx(fmaf(x[e], kLog2e, nmL));
-              acc1 += ex2_approx(fmaf(x[e + 1], kLog2e, nmL));
-            }
-          }
-        }
-        lse_combine(m, sum, smax, acc0 + acc1);
-      }
+      if (smax > -INFINITY) lse_combine(m, sum, smax, segment_exp_sum<T, NVL>(vb, nvec, lane, -smax * kLog2e));
       lmax = fmaxf(lmax, smax);
       // prune bound: before the list holds k keys, the k-th largest lane
-      // maximum (lane maxima are distinct elements); the block's shared
-      // maximum of its warps' bounds every segment (one shared load)
-      if (cnt < k) {
+      // maximum (lane maxima are distinct elements), sorted for only when at
+      // least k lane maxima lie above the current bound (else it cannot
+      // raise it); the block's shared maximum of its warps' bounds every
+      // segment (one shared load)
+      thr = fmaxf(thr, from_ordered_u32(*const_cast<volatile unsigned *>(&s_thr)));
+      if (cnt < k && __popc(__ballot_sync(0xffffffffu, lmax > thr)) >= k) {
         const float y = warp_sort_desc(lmax, lane);
         thr = fmaxf(thr, __shfl_sync(0xffffffffu, y, k - 1));
       }
-      thr = fmaxf(thr, from_ordered_u32(*const_cast<volatile unsigned *>(&s_thr)));
       if (!__any_sync(0xffffffffu, smax > -INFINITY && smax >= thr)) continue;
       unsigned cms[NVL];  // this lane's elements of each vector at or above the bound
       int mycnt = 0;
@@ -578,9 +614,10 @@ struct DraftPlan {
 
 // Few rows: 16-warp CTAs with 1024-token segments (bf16), when each row can
 // be split into parts of one segment per warp with every part resident at
-// once (one CTA per SM).  Otherwise 8-warp CTAs with 2048-token segments:
-// enough parts for about three CTAs per SM, but no part smaller than one
-// segment per warp.  At most kMaxDraftParts parts per row (one cluster).
+// once (one CTA per SM).  Otherwise 8-warp CTAs streaming 1024-token
+// segments through a shared-memory ring: enough parts for about three CTAs
+// per SM, but no part smaller than one segment per warp.  At most
+// kMaxDraftParts parts per row (one cluster).
 static DraftPlan draft_plan(int B, int R, int V, int vec, int num_sms) {
   const int64_t rows = static_cast<int64_t>(B) * R;
   DraftPlan p;
@@ -595,7 +632,7 @@ static DraftPlan draft_plan(int B, int R, int V, int vec, int num_sms) {
       return p;
     }
   }
-  const int seg = 8 * 32 * vec;
+  const int seg = 4 * 32 * vec;
   const int64_t nseg = (V + seg - 1) / seg;
   const int64_t max_parts = (nseg + 7) / 8;
   int64_t S = (static_cast<int64_t>(num_sms) * 3 + rows - 1) / rows;
@@ -603,7 +640,7 @@ static DraftPlan draft_plan(int B, int R, int V, int vec, int num_sms) {
   if (S > kMaxDraftParts) S = kMaxDraftParts;
   if (S < 1) S = 1;
   p.NW = 8;
-  p.NVL = 8;
+  p.NVL = 4;
   p.S = static_cast<int>(S);
   return p;
 }
@@ -612,12 +649,22 @@ static DraftPlan draft_plan(int B, int R, int V, int vec, int num_sms) {
 // workspace.
 size_t draft_workspace_bytes(int, int, int, int, int, int) { return 0; }
 
+// 8-warp CTAs: three ring stages of 4 vectors per lane for each warp
+constexpr int kRingBytes = 8 * 3 * 4 * 32 * 16;
+
 template <typename T>
 static cudaError_t launch_t(const DraftArgs &a, const DraftPlan &p, cudaStream_t st) {
   const dim3 grid(a.S, a.B * a.R);
   if (p.NW == 16)
     return launch_chained_cluster(draft_topk_kernel<T, 16, 4>, grid, dim3(16 * 32), 0, st, a.S, a);
-  return launch_chained_cluster(draft_topk_kernel<T, 8, 8>, grid, dim3(8 * 32), 0, st, a.S, a);
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(draft_topk_kernel<T, 8, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kRingBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  return launch_chained_cluster(draft_topk_kernel<T, 8, 4>, grid, dim3(8 * 32), kRingBytes, st, a.S, a);
 }
 
 cudaError_t launch_draft_topk(const void *logits, int dtype, int B, int D, int k, int V,
