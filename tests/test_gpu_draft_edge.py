@@ -8,7 +8,8 @@ tolerances.
 Shapes cover both launch forms: one sequence of Llama-2-7B-shaped rows
 (few rows: 16-warp CTAs, each row split over a cluster of CTAs) and four
 sequences (8-warp CTAs), in bf16 and fp32, plus k = 32 (also with every
-row split over an 8-CTA cluster).
+row split over an 8-CTA cluster), and many short rows whose 8-warp CTAs
+have fewer segments than warps or a one-vector last segment.
 """
 import numpy as np
 import pytest
@@ -56,6 +57,11 @@ CASES = [
     ("bf16", 1, 3, 32, 4096),
     ("bf16", 2, 2, 4, 201088),
     ("bf16", 1, 2, 32, 201088),     # 8-part clusters with k = 32: the part merge ranks 256 keys
+    # 8-warp CTAs streaming segments through the shared-memory ring:
+    ("bf16", 64, 6, 10, 4096),      # four segments per row: half the warps have none, the ring's
+                                    # look-ahead stages are empty copy groups
+    ("bf16", 16, 6, 10, 4104),      # a last segment of one 16-byte vector (lane 0 alone copies)
+    ("f32", 32, 4, 8, 1028),        # fp32 segments of 512 tokens, a one-vector tail
 ]
 
 
