@@ -145,6 +145,7 @@ __global__ void __launch_bounds__(NW * 32, NW <= 8 ? 3 : 1) draft_topk_kernel(Dr
   __shared__ __align__(8) uint64_t s_part_bar;                      // first CTA: the parts have pushed
   __shared__ uint64_t s_top[32];
   __shared__ float s_m[NW], s_s[NW];
+  __shared__ __align__(16) float s_lmax[NW * 32];  // ring form: each lane's running maximum
   __shared__ int s_nc;
   __shared__ unsigned s_thr;  // block prune bound (order-preserving bits)
 
@@ -214,6 +215,7 @@ __global__ void __launch_bounds__(NW * 32, NW <= 8 ? 3 : 1) draft_topk_kernel(Dr
     }
   }
   if (tid < 32) s_top[tid] = 0ull;
+  s_lmax[tid] = -INFINITY;
   __syncthreads();
   if (a.S > 1) cluster_arrive_relaxed();  // waited on before a part pushes to the first CTA
 
@@ -377,6 +379,29 @@ __global__ void __launch_bounds__(NW * 32, NW <= 8 ? 3 : 1) draft_topk_kernel(Dr
       }
       if (smax > -INFINITY) lse_combine(m, sum, smax, segment_exp_sum<T, NVL>(vb, nvec, lane, -smax * kLog2e));
       lmax = fmaxf(lmax, smax);
+      // block bound from the lanes' running maxima: a slot only ever holds an
+      // element of this part (or -inf), whenever it is read, and distinct
+      // slots hold distinct elements, so the k-th largest of any slots
+      // bounds the part's k-th largest from below.  Every fourth segment a
+      // warp takes the maxima of 32 groups of 8 slots and raises the shared
+      // bound to their k-th largest.
+      s_lmax[tid] = lmax;
+      if (((it + warp) & 3) == 0) {
+        float g[8];
+        asm volatile("ld.volatile.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(g[0]), "=f"(g[1]), "=f"(g[2]), "=f"(g[3]) : "r"(smem_u32(s_lmax + 8 * lane)));
+        asm volatile("ld.volatile.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(g[4]), "=f"(g[5]), "=f"(g[6]), "=f"(g[7]) : "r"(smem_u32(s_lmax + 8 * lane + 4)));
+        float gm = g[0];
+#pragma unroll
+        for (int e = 1; e < 8; ++e) gm = fmaxf(gm, g[e]);
+        const float y = warp_sort_desc(gm, lane);
+        const float kth = __shfl_sync(0xffffffffu, y, k - 1);
+        if (kth > thr) {
+          thr = kth;
+          if (lane == 0) atomicMax(&s_thr, ordered_u32(kth));
+        }
+      }
       // prune bound: before the list holds k keys, the k-th largest lane
       // maximum (lane maxima are distinct elements), sorted for only when at
       // least k lane maxima lie above the current bound (else it cannot
