@@ -5,6 +5,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 #include "../../include/eagle.h"
@@ -159,6 +160,23 @@ __device__ __forceinline__ void lse_combine(float &m, float &s, float m2, float 
   if (mn == -INFINITY) return;  // both empty
   s = s * ex2_approx((m - mn) * kLog2e) + s2 * ex2_approx((m2 - mn) * kLog2e);
   m = mn;
+}
+
+// ---- launch configuration ----------------------------------------------------
+// Raises a kernel's dynamic shared memory limit once per device (the limit
+// belongs to the kernel as loaded on the current device).  `done` is the
+// call site's record of the devices already configured: bit d for device
+// d < 64; devices beyond are configured on every call.
+template <typename Kernel>
+inline cudaError_t set_smem_limit_once(Kernel kernel, int bytes, std::atomic<unsigned long long> &done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev >= 0 && dev < 64 ? 1ull << dev : 0ull;
+  if (bit && (done.load(std::memory_order_relaxed) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_relaxed);
+  return e;
 }
 
 // ---- chained launches (programmatic dependent launch) --------------------

@@ -682,13 +682,9 @@ static cudaError_t launch_t(const DraftArgs &a, const DraftPlan &p, cudaStream_t
   const dim3 grid(a.S, a.B * a.R);
   if (p.NW == 16)
     return launch_chained_cluster(draft_topk_kernel<T, 16, 4>, grid, dim3(16 * 32), 0, st, a.S, a);
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(draft_topk_kernel<T, 8, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kRingBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<unsigned long long> configured{0};
+  const cudaError_t e = set_smem_limit_once(draft_topk_kernel<T, 8, 4>, kRingBytes, configured);
+  if (e != cudaSuccess) return e;
   return launch_chained_cluster(draft_topk_kernel<T, 8, 4>, grid, dim3(8 * 32), kRingBytes, st, a.S, a);
 }
 

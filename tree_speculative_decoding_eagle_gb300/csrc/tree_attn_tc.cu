@@ -765,13 +765,9 @@ static cudaError_t launch_tc_v(const CUtensorMap *maps, const TcArgs &a, const T
   static_assert(Sh::kSmem <= 232448, "shared memory budget");
   // MT = 1 variants run two CTAs per SM (228 KB per SM, 1 KB reserved per CTA)
   static_assert(MT != 1 || 2 * (Sh::kSmem + 1024) <= 233472, "two CTAs per SM");
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(tree_attn_tc_kernel<DH, MT, NK, STAGES, SPLIT, QR>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<unsigned long long> configured{0};
+  const cudaError_t e = set_smem_limit_once(tree_attn_tc_kernel<DH, MT, NK, STAGES, SPLIT, QR>, Sh::kSmem, configured);
+  if (e != cudaSuccess) return e;
   // the S splits of one (b, g, M-group) form one cluster
   dim3 grid(p.S, p.mgroups, a.B * a.Hkv);
   return launch_chained_cluster(tree_attn_tc_kernel<DH, MT, NK, STAGES, SPLIT, QR>, grid, dim3(Sh::kThreads), Sh::kSmem,
