@@ -14,13 +14,18 @@
 // memory (asynchronous copies issued two segments ahead, so the loads stay
 // in flight while a segment is being processed).  A warp visits each
 // segment twice: lane maxima, then the sum of exp(x - segment max), folded
-// into a running (max, sum).  Top-k selection works on unique 64-bit keys (logit order,
-// then lower token id).  Each warp keeps its k best keys so far sorted in
-// registers (lane i holds the i-th); a new key's place is the number of
-// larger keys (one ballot) and the tail shifts down one lane.  The list's
-// k-th key bounds the part from below, so values under the bound (shared
-// block-wide as a maximum over the warps) are never looked at; before the
-// list is full, the k-th largest lane maximum is the bound.  The warp lists
+// into a running (max, sum).  Top-k selection works on unique 64-bit keys
+// (logit order, then lower token id).  Each warp keeps its k best keys so
+// far sorted in registers (lane i holds the i-th); a new key's place is the
+// number of larger keys (one ballot) and the tail shifts down one lane.  The
+// list's k-th key bounds the part from below, so values under the bound
+// (shared block-wide as a maximum over the warps) are never looked at;
+// before the list is full, the k-th largest lane maximum is the bound.  In
+// the ring form the lanes also keep their running maxima in shared memory,
+// and every fourth segment a warp raises the shared bound to the k-th
+// largest of their group maxima (distinct elements, so a valid bound
+// whenever read): the bound then reflects the whole block's progress
+// rather than one warp's share of the row.  The warp lists
 // merge block-wide: only keys at or above the block's bound are kept, and
 // their ranks are counted.  With S > 1 every part pushes its k keys and
 // (max, sum) into the shared memory of the row's first CTA and signals its
