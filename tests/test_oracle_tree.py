@@ -257,6 +257,26 @@ def test_closure_adds_ancestors_outside_the_probability_domain():
     assert token_paths(out) == {(6,), (6, 3)}
 
 
+def test_negative_zero_confidence_ranks_as_zero():
+    """A confidence of -0 compares equal to +0 (IEEE), so the key order, the
+    expansion and the kept set are those of the same rows with +0; the
+    scores differ at most in the sign of zero."""
+    rng = np.random.default_rng(21)
+    D, k, m = 4, 4, 30
+    tok = np.stack([np.stack([rng.choice(50, size=k, replace=False) for _ in range(k)]) for _ in range(D)])
+    conf = (rng.integers(0, 3, size=(D, k, k)) / 4.0).astype(np.float32)   # many zeros, many ties
+    neg = conf.copy()
+    neg[conf == 0] = np.float32(-0.0)
+    assert np.signbit(neg).any()
+    for confidence_only, rerank in [(False, True), (True, True), (False, False)]:
+        mm = min(m, D * k) if not rerank else m
+        a = otree.build_tree(tok, conf, mm, confidence_only=confidence_only, rerank=rerank)
+        b = otree.build_tree(tok, neg, mm, confidence_only=confidence_only, rerank=rerank)
+        for key in ("tok", "parent", "depth", "src", "row"):
+            assert (a[key] == b[key]).all(), key
+        assert (a["score"] == b["score"]).all()          # -0 == +0
+
+
 def test_build_trees_batch_matches_single():
     rng = np.random.default_rng(7)
     toks, confs = zip(*[random_rows(rng, 3, 3, 20) for _ in range(3)])
