@@ -103,21 +103,6 @@ int eagle_draft_topk(const void *logits, int dtype, int B, int D, int k, int V,
                      eagle_stream_t stream);
 
 /* ------------------------------------------------------------------------
- * Stage 1 without caller scratch: eagle_draft_topk_noalloc.
- * The paper has no counterpart to this entry point; it exists for callers
- * that cannot give the library scratch memory — plugins or custom-op hooks
- * of a host runtime that hands over only input and output buffers and owns
- * all device memory, or processes whose device-memory budget is fixed up
- * front.  Same arguments and results as eagle_draft_topk, without the
- * workspace arguments (the stage needs none).  It allocates nothing; calls
- * on different streams may overlap.
- * ------------------------------------------------------------------------ */
-int eagle_draft_topk_noalloc(const void *logits, int dtype, int B, int D, int k,
-                             int V, int64_t ld, int32_t *tok, float *conf,
-                             float *stats, int32_t *status,
-                             eagle_stream_t stream);
-
-/* ------------------------------------------------------------------------
  * Stage 2 — dynamic draft tree.
  * [EAGLE-2] section "動的ドラフトツリーの構築アルゴリズム": V_i = product of
  * the confidences on the root path (V_i equation); at every depth the k
@@ -336,6 +321,43 @@ int eagle_verify(const void *target, int dtype, int64_t ld,
                  int32_t *path_nodes, int32_t *out_tokens, int32_t *status,
                  void *workspace, size_t workspace_bytes,
                  eagle_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Stage 4 without caller scratch: eagle_verify_noalloc.
+ * The paper has no counterpart to this entry point.  It serves callers that
+ * cannot allocate device memory for a workspace: a plugin or custom-op hook
+ * inside a host runtime that owns every device buffer and hands the op only
+ * its inputs and outputs; a serving loop that must not call cudaMalloc once
+ * it is running (cudaMalloc can synchronise the device and stall the work
+ * in flight); a process whose device memory is all handed to its own pool.
+ * Same arguments, results and device errors as eagle_verify, without the
+ * workspace arguments.  The per-chunk statistics records that eagle_verify
+ * keeps in its workspace live instead in one array inside the library
+ * (a file-scope __device__ array of EAGLE_VERIFY_NOALLOC_SCRATCH_BYTES
+ * bytes), which every GPU that loads the library holds until the process
+ * exits.  Nothing is allocated by the call itself.
+ *   - A request whose records exceed the array (eagle_verify_workspace_size
+ *     > EAGLE_VERIFY_NOALLOC_SCRATCH_BYTES) returns EAGLE_ERR_WORKSPACE and
+ *     launches nothing.  8 MiB covers B * (m+1) * ceil(V/2048) <= 524288
+ *     records, e.g. B = 64, m = 60, V = 201088.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and keeps it; make that first call before any
+ *     stream capture.
+ *   - Every call shares the one array, and it keeps the last call's
+ *     records.  No record needs clearing: each call writes every record it
+ *     reads.  Two calls that may overlap on the GPU (on different streams
+ *     without an ordering between them, or on one device from two threads
+ *     through unordered streams) race on the array and give wrong results.
+ * ------------------------------------------------------------------------ */
+#define EAGLE_VERIFY_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+int eagle_verify_noalloc(const void *target, int dtype, int64_t ld,
+                         const int32_t *node_tok, const int32_t *node_parent,
+                         int B, int m, int D, int V, int mode,
+                         float temperature, const float *uniforms,
+                         int32_t *accept_len, int32_t *path_nodes,
+                         int32_t *out_tokens, int32_t *status,
+                         eagle_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Stage 4 with draft distributions — speculative-sampling verification of a

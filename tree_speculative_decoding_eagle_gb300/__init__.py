@@ -15,6 +15,7 @@ library is missing or a call reports an error, an exception is raised.
     tree_attn_paged -> eagle_tree_attn_paged (the same over a paged prefix)
     kv_commit   -> eagle_kv_commit    (accepted path's K/V into the cache)
     verify      -> eagle_verify       (greedy / speculative-sampling walk)
+    verify_noalloc -> eagle_verify_noalloc (the same without a caller workspace)
     verify_draft -> eagle_verify_draft (sampling walk against draft distributions q)
 """
 import ctypes
@@ -31,11 +32,11 @@ TREE_CONFIDENCE_ONLY, TREE_NO_RERANK = 1, 2
 
 EXPORTED = (
     "eagle_status_string", "eagle_version",
-    "eagle_draft_topk_workspace_size", "eagle_draft_topk", "eagle_draft_topk_noalloc",
+    "eagle_draft_topk_workspace_size", "eagle_draft_topk",
     "eagle_tree_build", "eagle_tree_build_variant", "eagle_static_tree", "eagle_tree_mask",
     "eagle_tree_attn_workspace_size", "eagle_tree_attn",
     "eagle_tree_attn_paged_workspace_size", "eagle_tree_attn_paged", "eagle_kv_commit",
-    "eagle_verify_workspace_size", "eagle_verify", "eagle_verify_draft",
+    "eagle_verify_workspace_size", "eagle_verify", "eagle_verify_noalloc", "eagle_verify_draft",
 )
 
 _lib = None
@@ -59,7 +60,6 @@ def load_library(path=LIB_PATH):
         "eagle_version": (I, []),
         "eagle_draft_topk_workspace_size": (SZ, [I, I, I, I]),
         "eagle_draft_topk": (I, [P, I, I, I, I, I, I64, P, P, P, P, P, SZ, P]),
-        "eagle_draft_topk_noalloc": (I, [P, I, I, I, I, I, I64, P, P, P, P, P]),
         "eagle_tree_build": (I, [P, P, I, I, I, I, P, P, P, P, P, P, P, P, P, P]),
         "eagle_tree_build_variant": (I, [P, P, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P]),
         "eagle_static_tree": (I, [P, P, I, I, I, P, P, I, P, P, P, P, P, P, P, P, P, P]),
@@ -71,6 +71,7 @@ def load_library(path=LIB_PATH):
         "eagle_kv_commit": (I, [P, P, I, I, I, I, I, P, P, I, P, P, I, P, I, I, I, P, P, P, P]),
         "eagle_verify_workspace_size": (SZ, [I, I, I]),
         "eagle_verify": (I, [P, I, I64, P, P, I, I, I, I, I, F, P, P, P, P, P, P, SZ, P]),
+        "eagle_verify_noalloc": (I, [P, I, I64, P, P, I, I, I, I, I, F, P, P, P, P, P, P]),
         "eagle_verify_draft": (I, [P, P, I, I64, I64, P, P, P, I, I, I, I, I, F, P, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
@@ -146,27 +147,6 @@ def draft_topk(logits, k, tok=None, conf=None, stats=None, workspace=None, statu
                                 _ptr(conf), _ptr(stats), _ptr(status), _ptr(wbuf), wbytes,
                                 _stream(stream)),
            "eagle_draft_topk")
-    return tok, conf, stats
-
-
-def draft_topk_noalloc(logits, k, tok=None, conf=None, stats=None, status=None, stream=None):
-    """draft_topk for callers that cannot provide scratch memory: the library
-    uses its own fixed scratch array (calls that overlap on the GPU race)."""
-    lib = load_library()
-    _cuda(logits, "logits")
-    B, D, kk, V = logits.shape
-    if kk != k or logits.stride(-1) != 1:
-        raise EagleError("logits must be [B, D, k, V] with unit stride in V")
-    ld = logits.stride(2)
-    if logits.stride(1) != k * ld or logits.stride(0) != D * k * ld:
-        raise EagleError("logits rows must be evenly spaced")
-    dev = logits.device
-    tok = tok if tok is not None else torch.empty((B, D, k, k), dtype=torch.int32, device=dev)
-    conf = conf if conf is not None else torch.empty((B, D, k, k), dtype=torch.float32, device=dev)
-    stats = stats if stats is not None else torch.empty((B, D, k, 2), dtype=torch.float32, device=dev)
-    _check(lib.eagle_draft_topk_noalloc(_ptr(logits), _dtype_code(logits), B, D, k, V, ld, _ptr(tok),
-                                        _ptr(conf), _ptr(stats), _ptr(status), _stream(stream)),
-           "eagle_draft_topk_noalloc")
     return tok, conf, stats
 
 
@@ -287,6 +267,28 @@ def verify(target, node_tok, node_parent, D, mode, temperature=1.0, uniforms=Non
     return accept_len, path_nodes, out_tokens
 
 
+def verify_noalloc(target, node_tok, node_parent, D, mode, temperature=1.0, uniforms=None,
+                   accept_len=None, path_nodes=None, out_tokens=None, status=None, stream=None):
+    """verify() for callers that cannot allocate device memory for a workspace
+    (eagle_verify_noalloc): the chunk records live in a fixed array inside the
+    library, so calls that overlap on the GPU race.  Same results as verify()."""
+    lib = load_library()
+    _cuda(target, "target")
+    B, n, V = target.shape
+    if target.stride(-1) != 1 or target.stride(0) != n * target.stride(1):
+        raise EagleError("target must be [B, m+1, V] with evenly spaced rows")
+    dev = target.device
+    accept_len = accept_len if accept_len is not None else torch.empty(B, dtype=torch.int32, device=dev)
+    path_nodes = path_nodes if path_nodes is not None else torch.empty((B, D + 1), dtype=torch.int32, device=dev)
+    out_tokens = out_tokens if out_tokens is not None else torch.empty((B, D + 1), dtype=torch.int32, device=dev)
+    mode_code = GREEDY if mode in ("greedy", GREEDY) else SAMPLE
+    _check(lib.eagle_verify_noalloc(_ptr(target), _dtype_code(target), target.stride(1), _ptr(node_tok),
+                                    _ptr(node_parent), B, n - 1, D, V, mode_code, ctypes.c_float(temperature),
+                                    _ptr(uniforms), _ptr(accept_len), _ptr(path_nodes), _ptr(out_tokens),
+                                    _ptr(status), _stream(stream)), "eagle_verify_noalloc")
+    return accept_len, path_nodes, out_tokens
+
+
 def verify_draft(target, draft, node_tok, node_parent, node_row, D, temperature, uniforms, accept_len=None,
                  path_nodes=None, out_tokens=None, status=None, stream=None):
     """Speculative-sampling verification against the draft distributions:
@@ -353,3 +355,4 @@ def kv_commit(k_tree, v_tree, accept_len, path_nodes, k_cache, v_cache, kv_len, 
                                max_pages, page_size, num_pages, _ptr(kv_len), _ptr(slot_mapping), _ptr(status),
                                _stream(stream)), "eagle_kv_commit")
     return slot_mapping
+
