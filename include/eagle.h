@@ -19,10 +19,11 @@
  * Conventions for every entry point:
  *   - All array pointers are DEVICE pointers owned by the caller; the library
  *     never allocates, frees or keeps them.  Scratch memory is passed in as
- *     `workspace` (size from the matching *_workspace_size query); it must be
- *     zero-filled before its first use, and every call leaves it zeroed where
- *     that matters (its split-merge counters), so it can be reused as is.
- *     One workspace must not be used by two calls that may overlap on the GPU.
+ *     `workspace` (size from the matching *_workspace_size query; a size of
+ *     0 means the call needs none).  A workspace needs no initialisation and
+ *     keeps no state between calls: a call writes every byte of it that it
+ *     reads.  One workspace must not be used by two calls that may overlap
+ *     on the GPU.
  *   - Every call is asynchronous on `stream` (NULL = the legacy default
  *     stream).  The return value reports argument and launch errors only:
  *     EAGLE_OK, EAGLE_ERR_INVALID (bad argument, nothing launched),
@@ -68,6 +69,27 @@ const char *eagle_status_string(int code);
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 int eagle_version(void);
+
+/* ------------------------------------------------------------------------
+ * Self test of the bounded device waits (failure detection).
+ * The pages describe no failure handling; this call checks the library's
+ * own.  Every wait inside the step's kernels (on an mbarrier completed by a
+ * copy, an MMA or another CTA of a cluster) gives up after a wall-time
+ * limit, and the kernel then reports EAGLE_ERR_TIMEOUT in the status word
+ * instead of hanging.  This launches one warp that initialises an mbarrier
+ * nothing will ever complete and waits on it with the same helper the
+ * kernels use, for `limit_ns` nanoseconds:
+ *   which       0: the CTA-local wait; 1: the polling wait used for
+ *               barriers that other CTAs of a cluster arrive on
+ *   status      device int32 (required): EAGLE_ERR_TIMEOUT when the wait
+ *               gave up as designed, EAGLE_ERR_INVALID if it returned as
+ *               though the barrier had completed
+ *   elapsed_ns  device uint64 (out; may be NULL): the wall time waited
+ * Nothing else is in flight, so the context stays usable afterwards.
+ * Limits: 1000 <= limit_ns <= 100000000 (1 us to 100 ms).
+ * ------------------------------------------------------------------------ */
+int eagle_selftest_wait(uint64_t limit_ns, int which, int32_t *status,
+                        uint64_t *elapsed_ns, eagle_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Stage 1 — draft softmax statistics and top-k.
@@ -308,7 +330,10 @@ int eagle_tree_attn_paged(const void *q, const void *k_pages,
  *   path_nodes device int32 [B, D+1]       (out; root first; -1 padded)
  *   out_tokens device int32 [B, D+1]       (out; accepted tokens, then the
  *                                           bonus token; -1 padded)
- *   status     device int32 (out; may be NULL)
+ *   status     device int32 (out; may be NULL): EAGLE_ERR_INVALID when the
+ *              walk meets a row with no finite logit (greedy: no argmax) or
+ *              with no residual mass (sampling), or a child token outside
+ *              [0, V) (sampling); the bonus token is then -1
  * D bounds the tree depth.  Limits: V*elemsize and ld*elemsize multiples of
  * 16 bytes; 1 <= m+1 <= 4096; D >= 1.
  * ------------------------------------------------------------------------ */

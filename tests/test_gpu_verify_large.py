@@ -77,3 +77,29 @@ def test_verify_large_tree(m, mode):
         checked += 1
     assert checked >= 1
     assert acc_o.max() >= 1          # the planted paths make walks take steps
+
+
+@pytest.mark.parametrize("where", ["root", "second"])
+def test_greedy_row_without_finite_logit_sets_status(where):
+    """A target row with no finite logit has no argmax.  The greedy walk stops
+    at that row with bonus -1 and reports EAGLE_ERR_INVALID; the path up to
+    that row is the oracle's (computed on the rows before the bad one)."""
+    B, n, D, V = 1, 40, 5, 4096
+    rng = np.random.default_rng(3100 + (where == "second"))
+    par, tok, logits = planted_trees(B, n, D, V, rng)
+    acc_o, path_o, _, _ = over.verify(logits, tok, par, D, "greedy")
+    bad = 0 if where == "root" else int(path_o[0, 1])
+    assert bad >= 0
+    logits[0, bad, :] = -np.inf
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    acc, path, toks = eg.verify(torch.from_numpy(logits).to(torch.bfloat16).cuda(),
+                                torch.from_numpy(tok.astype(np.int32)).cuda(),
+                                torch.from_numpy(par.astype(np.int32)).cuda(), D, "greedy", status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == -1
+    a = 0 if where == "root" else 1
+    assert int(acc[0]) == a
+    assert path[0, :a + 1].tolist() == path_o[0, :a + 1].tolist()
+    assert (path[0, a + 1:] == -1).all()
+    assert toks[0, :a].tolist() == [int(tok[0, p]) for p in path_o[0, 1:a + 1]]
+    assert (toks[0, a:] == -1).all()

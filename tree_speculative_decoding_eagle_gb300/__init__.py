@@ -17,6 +17,7 @@ library is missing or a call reports an error, an exception is raised.
     verify      -> eagle_verify       (greedy / speculative-sampling walk)
     verify_noalloc -> eagle_verify_noalloc (the same without a caller workspace)
     verify_draft -> eagle_verify_draft (sampling walk against draft distributions q)
+    selftest_wait -> eagle_selftest_wait (a bounded device wait that must give up)
 """
 import ctypes
 import os
@@ -31,7 +32,7 @@ GREEDY, SAMPLE = 0, 1
 TREE_CONFIDENCE_ONLY, TREE_NO_RERANK = 1, 2
 
 EXPORTED = (
-    "eagle_status_string", "eagle_version",
+    "eagle_status_string", "eagle_version", "eagle_selftest_wait",
     "eagle_draft_topk_workspace_size", "eagle_draft_topk",
     "eagle_tree_build", "eagle_tree_build_variant", "eagle_static_tree", "eagle_tree_mask",
     "eagle_tree_attn_workspace_size", "eagle_tree_attn",
@@ -58,6 +59,7 @@ def load_library(path=LIB_PATH):
     sig = {
         "eagle_status_string": (ctypes.c_char_p, [I]),
         "eagle_version": (I, []),
+        "eagle_selftest_wait": (I, [ctypes.c_uint64, I, P, P, P]),
         "eagle_draft_topk_workspace_size": (SZ, [I, I, I, I]),
         "eagle_draft_topk": (I, [P, I, I, I, I, I, I64, P, P, P, P, P, SZ, P]),
         "eagle_tree_build": (I, [P, P, I, I, I, I, P, P, P, P, P, P, P, P, P, P]),
@@ -356,3 +358,16 @@ def kv_commit(k_tree, v_tree, accept_len, path_nodes, k_cache, v_cache, kv_len, 
                                _stream(stream)), "eagle_kv_commit")
     return slot_mapping
 
+
+def selftest_wait(limit_ns=1_000_000, which=0, stream=None):
+    """Runs eagle_selftest_wait: one warp waits on an mbarrier that nothing
+    completes, with the kernels' own bounded-wait helper.  Returns (status
+    code written by the device, nanoseconds waited); the status is
+    EAGLE_ERR_TIMEOUT (-5) when the wait gave up as designed."""
+    lib = load_library()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    elapsed = torch.zeros(1, dtype=torch.int64, device="cuda")
+    _check(lib.eagle_selftest_wait(int(limit_ns), int(which), _ptr(status), _ptr(elapsed), _stream(stream)),
+           "eagle_selftest_wait")
+    (stream or torch.cuda.current_stream()).synchronize()
+    return int(status.item()), int(elapsed.item())

@@ -163,6 +163,7 @@ __device__ __forceinline__ void lse_combine(float &m, float &s, float m2, float 
 }
 
 // ---- launch configuration ----------------------------------------------------
+
 // Raises a kernel's dynamic shared memory limit once per device (the limit
 // belongs to the kernel as loaded on the current device).  `done` is the
 // call site's record of the devices already configured: bit d for device
@@ -174,6 +175,29 @@ inline cudaError_t set_smem_limit_once(Kernel kernel, int bytes, std::atomic<uns
   if (e != cudaSuccess) return e;
   const unsigned long long bit = dev >= 0 && dev < 64 ? 1ull << dev : 0ull;
   if (bit && (done.load(std::memory_order_relaxed) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_relaxed);
+  return e;
+}
+
+// Raises a kernel's dynamic shared memory limit, once per device, to the
+// most it can take: the device's opt-in maximum per block less the kernel's
+// static shared memory.  The limit then only ever grows, so host threads
+// launching the kernel with different sizes cannot lower it under each other.
+template <typename Kernel>
+inline cudaError_t set_smem_limit_max_once(Kernel kernel, std::atomic<unsigned long long> &done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev >= 0 && dev < 64 ? 1ull << dev : 0ull;
+  if (bit && (done.load(std::memory_order_relaxed) & bit)) return cudaSuccess;
+  int optin = 0;
+  e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, kernel);
+  if (e != cudaSuccess) return e;
+  const int bytes = optin - static_cast<int>(fa.sharedSizeBytes);
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_relaxed);
   return e;

@@ -150,8 +150,8 @@ cudaError_t launch_static_tree(const int32_t *tok, const float *conf, int B, int
   a.mask = mask; a.status = status;
   const size_t smem = sizeof(int) * 5 * static_cast<size_t>(n);
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(static_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    static std::atomic<unsigned long long> configured{0};  // raised once per device, to the maximum
+    const cudaError_t e = set_smem_limit_max_once(static_tree_kernel, configured);
     if (e != cudaSuccess) return e;
   }
   static_tree_kernel<<<B, kStaticThreads, smem, st>>>(a);

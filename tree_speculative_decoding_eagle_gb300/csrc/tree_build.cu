@@ -380,8 +380,10 @@ cudaError_t launch_tree_build(const int32_t *tok, const float *conf, int B, int 
   a.mask = mask; a.status = status;
   const size_t smem = tree_smem_bytes(D, k, m);
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(tree_build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    // the limit is raised once per device to the opt-in maximum, so it only
+    // ever grows (two host threads with different sizes cannot undo each other)
+    static std::atomic<unsigned long long> configured{0};
+    const cudaError_t e = set_smem_limit_max_once(tree_build_kernel, configured);
     if (e != cudaSuccess) return e;
   }
   return launch_chained(tree_build_kernel, dim3(B), dim3(kTreeThreads), smem, st, a);

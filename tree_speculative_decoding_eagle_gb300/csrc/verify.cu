@@ -199,7 +199,10 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(VerifyArgs a)
     if (!sample) {
       bonus = static_cast<int>(__reduce_min_sync(
           0xffffffffu, ordered_u32(bm) == om ? static_cast<uint32_t>(ba) : 0xffffffffu));
-      for (int base = 0; base < n && next < 0; base += 32) {
+      // a row with no finite logit (all -inf, or NaN) has no argmax: the walk
+      // stops here with bonus -1 and reports EAGLE_ERR_INVALID below
+      if (bonus < 0 || bonus >= a.V) bonus = -1;
+      for (int base = 0; bonus >= 0 && base < n && next < 0; base += 32) {
         const int i = base + lane;
         const bool hit = i < n && s_par[i] == cur && s_tok[i] == bonus;
         const unsigned bal = __ballot_sync(0xffffffffu, hit);
@@ -409,8 +412,8 @@ static cudaError_t launch_verify_t(const VerifyArgs &a, int num_sms, cudaStream_
   size_t smem = sizeof(int) * 7 * static_cast<size_t>(a.n);
   if (a.stage_stats) smem += sizeof(ChunkStat) * static_cast<size_t>(a.n) * a.nch;
   if (smem > 48 * 1024) {
-    e = cudaFuncSetAttribute(verify_walk_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
+    static std::atomic<unsigned long long> configured{0};  // raised once per device, to the maximum
+    e = set_smem_limit_max_once(verify_walk_kernel<T>, configured);
     if (e != cudaSuccess) return e;
   }
   return launch_chained(verify_walk_kernel<T>, dim3(a.B), dim3(kWalkThreads), smem, st, a);
