@@ -32,6 +32,7 @@ class Case:
     w: gen.Workload
     oracle_seqs: list            # sequences the oracle computes fully
     attn_samples: object = None  # None = all outputs, else list of (b, i, h)
+    attn_groups: list = field(default_factory=list)  # (b, KV head g): every node x grouped head compared
     device: str = "cuda"
     extra: dict = field(default_factory=dict)
 
@@ -132,3 +133,15 @@ def compare_walk(w, mode, acc_g, path_g, tok_g, want, seqs):
             pos = r.ambiguous[0]
             assert (path_g[b, :pos + 1] == path_o[b, :pos + 1]).all(), b
     return n_amb
+
+
+def attn_group_expected(ai_cpu, masks_bool, b, g, G, scale):
+    """The oracle's outputs for every (node, grouped head) of one sequence b
+    and KV head g: out [n, G, dh] and lse [n, G]."""
+    sl = slice(g * G, (g + 1) * G)
+    q = f64(ai_cpu["q"][b:b + 1, :, sl])
+    kc, vc = f64(ai_cpu["k_cache"][b:b + 1, g:g + 1]), f64(ai_cpu["v_cache"][b:b + 1, g:g + 1])
+    kt, vt = f64(ai_cpu["k_tree"][b:b + 1, g:g + 1]), f64(ai_cpu["v_tree"][b:b + 1, g:g + 1])
+    kv = ai_cpu["kv_len"].cpu().numpy()[b:b + 1]
+    o, l = oattn.tree_attention(q, kc, vc, kv, kt, vt, masks_bool[b:b + 1], scale)
+    return o[0], l[0]

@@ -162,3 +162,49 @@ def test_kv_commit_past_capacity_sets_status():
     eg.kv_commit(tree, tree, acc, path, ck, ck.clone(), kl, status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == -1 and int(kl.item()) == 7 and float(ck.abs().sum()) == 0.0
+
+
+def test_paged_attention_full_size_whole_groups():
+    """70B-shaped GQA 8 at its full batch (16 sequences, 4096-token prefix,
+    the unsplit two-M-tile launch), prefix in 64-token pages behind a
+    shuffled block table built on the device: bit-identical to the
+    contiguous kernel everywhere, and every (node, grouped head) output of
+    whole (sequence, KV head) groups within the bf16 tolerance of the
+    oracle."""
+    from paritylib import attn_group_expected
+    w = gen.WORKLOADS["llama2-70b-b16"]
+    ai = gen.attention_inputs(w, device="cuda")
+    B, Hkv, Lmax, dh = ai["k_cache"].shape
+    P = 64
+    mp = Lmax // P
+    num_pages = B * mp + 16
+    gcpu = torch.Generator().manual_seed(1900)
+    table = torch.randperm(num_pages, generator=gcpu)[:B * mp].view(B, mp).to(torch.int32).cuda()
+    idx = table.reshape(-1).long()
+
+    def pool(cache):
+        p = torch.zeros((num_pages, Hkv, P, dh), dtype=cache.dtype, device="cuda")
+        p[idx] = cache.view(B, Hkv, mp, P, dh).permute(0, 2, 1, 3, 4).reshape(B * mp, Hkv, P, dh)
+        return p
+
+    kp, vp = pool(ai["k_cache"]), pool(ai["v_cache"])
+    n = w.n_nodes
+    masks = random_tree_mask(n, B, 1901)
+    mask_gpu = torch.from_numpy(omask.pack_mask(masks).view(np.int64)).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out_p, lse_p = eg.tree_attn_paged(ai["q"], kp, vp, table, ai["kv_len"], ai["k_tree"], ai["v_tree"],
+                                      mask_gpu, status=status)
+    out_c, lse_c = eg.tree_attn(ai["q"], ai["k_cache"], ai["v_cache"], ai["kv_len"], ai["k_tree"],
+                                ai["v_tree"], mask_gpu)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(out_p, out_c) and torch.equal(lse_p, lse_c)
+    del kp, vp
+    ai_cpu = {k: v.cpu() for k, v in ai.items()}
+    G = w.Hq // w.Hkv
+    got = out_p.double().cpu().numpy()
+    lse = lse_p.cpu().numpy()
+    for (b, g) in ((0, 0), (B - 1, Hkv - 1), (9, 2)):
+        o, l = attn_group_expected(ai_cpu, masks, b, g, G, dh ** -0.5)
+        assert np.abs(got[b, :, g * G:(g + 1) * G] - o).max() <= 2e-2, (b, g)
+        assert np.abs(lse[b, :, g * G:(g + 1) * G] - l).max() <= 1e-3, (b, g)

@@ -23,8 +23,8 @@ from oracle import draft as odraft
 from oracle import mask as omask
 from oracle import verify as over
 
-from paritylib import (ATTN_TOL, LSE_TOL, Case, attn_expected, compare_draft, compare_tree,
-                       compare_walk, f64, fill_trees, near_tie, oracle_tree_stage)
+from paritylib import (ATTN_TOL, LSE_TOL, Case, attn_expected, attn_group_expected, compare_draft,
+                       compare_tree, compare_walk, f64, fill_trees, near_tie, oracle_tree_stage)
 
 pytestmark = pytest.mark.gpu
 
@@ -48,12 +48,16 @@ CASES = {
     "llama2-13b-b8": Case(W["llama2-13b-b8"], list(range(8)),
                           attn_samples=[(b, i, h) for b in (0, 5, 7) for i in (0, 17, 50)
                                         for h in (0, 39)]),
+    # GQA 8: rows are (node, grouped head) pairs; whole groups cover every
+    # 128-row M-tile of the launch, the sampled outputs other sequences
     "llama2-70b-b16": Case(W["llama2-70b-b16"], list(range(16)),
                            attn_samples=[(b, i, h) for b in (0, 9, 15) for i in (0, 23, 48)
-                                         for h in (0, 7, 8, 63)]),
+                                         for h in (0, 7, 8, 63)],
+                           attn_groups=[(0, 0), (15, 7), (6, 3)]),
     "gpt-oss-20b-b64": Case(W["gpt-oss-20b-b64"], [0, 21, 63],
                             attn_samples=[(b, i, h) for b in (0, 33, 63) for i in (0, 30, 60)
-                                          for h in (0, 15, 63)]),
+                                          for h in (0, 15, 63)],
+                            attn_groups=[(0, 0), (63, 7), (33, 4)]),
 }
 
 
@@ -131,6 +135,11 @@ def run_case(case):
         for (b, i, h), (o, l) in exp.items():
             assert np.abs(out_g[b, i, h] - o).max() <= tol, (b, i, h)
             assert abs(lse_g[b, i, h] - l) <= LSE_TOL, (b, i, h)
+    G = w.Hq // w.Hkv
+    for (b, g) in case.attn_groups:
+        o, l = attn_group_expected(ai_cpu, masks_bool, b, g, G, w.dh ** -0.5)
+        assert np.abs(out_g[b, :, g * G:(g + 1) * G] - o).max() <= tol, (b, g)
+        assert np.abs(lse_g[b, :, g * G:(g + 1) * G] - l).max() <= LSE_TOL, (b, g)
     del ai_gpu, ai
 
     # ---- stage 4: verification -------------------------------------------------
