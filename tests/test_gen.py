@@ -78,3 +78,19 @@ def test_workload_derived_sizes():
     assert w.n_candidates == 510 and w.rows_used == 51 and w.n_nodes == 61
     w = WORKLOADS["gpt-oss-20b-b64"]
     assert w.n_candidates == 610 and w.rows_used == 61
+
+
+def test_philox_known_answers(golden_dir):
+    """The generator reproduces Philox4x32-10's published known-answer
+    vectors (zero, all-ones and pi-digit counters and keys), so every round
+    constant, multiplier and word permutation is as defined."""
+    import os
+    rows = []
+    with open(os.path.join(golden_dir, "philox4x32_10_kat.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                rows.append([int(x, 16) for x in line.split()])
+    assert len(rows) == 3
+    for r in rows:
+        out = philox4x32_10(np.array(r[:4], dtype=np.uint64), r[4:6])
+        assert out.tolist() == r[6:10], [hex(x) for x in out.tolist()]
