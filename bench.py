@@ -34,7 +34,10 @@ if "--cpu-worker" in sys.argv or "reference" in sys.argv:
         os.environ[_v] = "1"
 
 MAIN_WORKLOAD = "llama2-7b-b1"      # B=1, Llama-2-7B-shaped
-ALSO_WORKLOAD = "gpt-oss-20b-b64"   # B=64, GPT-OSS-20B-shaped high concurrency
+# the other bf16 workloads, each reported in the line's `also` list:
+# B=8 Llama-2-13B-shaped (ragged prefixes, sampling), B=16 Llama-2-70B-shaped
+# (GQA 8, greedy), B=64 GPT-OSS-20B-shaped high concurrency (sampling)
+ALSO_WORKLOADS = "llama2-13b-b8,llama2-70b-b16,gpt-oss-20b-b64"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 STAGE_LAUNCHES = 10   # launches per stage-timing graph
 
@@ -47,7 +50,8 @@ def parse_args(argv=None):
     p.add_argument("--workload", default=MAIN_WORKLOAD)
     p.add_argument("--batch", type=int, default=None,
                    help="run the workload at this batch size instead of its own (small ncu captures)")
-    p.add_argument("--also", default=ALSO_WORKLOAD, help="second workload reported in the line ('none' to skip)")
+    p.add_argument("--also", default=ALSO_WORKLOADS,
+                   help="comma-separated further workloads reported in the line ('none' to skip)")
     p.add_argument("--impl", default="ours", choices=("ours", "reference"))
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -630,17 +634,21 @@ def main(argv=None):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = run_cpu_baseline(args.workload, args.cpu_seconds)
     res = bench_workload(w, args, rank, world, device, with_e2e=not args.no_e2e, next_rows=not args.no_next_rows)
-    also = None
-    if args.also and args.also != "none" and args.also != args.workload:
-        w2 = gen.WORKLOADS[args.also]
+    also = []
+    names = [] if args.also in ("", "none") else [x for x in args.also.split(",") if x and x != args.workload]
+    for nm in names:
+        w2 = gen.WORKLOADS[nm]
+        torch.cuda.empty_cache()
         r2 = bench_workload(w2, args, rank, world, device, with_e2e=False)
-        also = {"workload": w2.name, "value": round(r2["value"], 2), "unit": "steps/s",
-                "ms_per_step": round(r2["ms_per_step"], 5),
-                "step_gbs": round(r2["step_bytes"] / (r2["ms_per_step"] * 1e-3) / 1e9, 1),
-                "step_hbm_frac": round(r2["step_bytes"] / (r2["ms_per_step"] * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
-                "roofline": roofline(r2, peaks, peak_src, w2.name),
-                "stages": stage_table(r2, peaks), "mean_accept_len": r2["tau"],
-                "clocks": r2["clocks"]}
+        gbs = r2["step_bytes"] / (r2["ms_per_step"] * 1e-3) / 1e9
+        also.append({"workload": w2.name, "B": w2.B, "mode": w2.modes[0],
+                     "value": round(r2["value"], 2), "unit": "steps/s",
+                     "ms_per_step": round(r2["ms_per_step"], 5), "step_bytes": r2["step_bytes"],
+                     "step_gbs": round(gbs, 1), "step_hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+                     "roofline": roofline(r2, peaks, peak_src, w2.name),
+                     "stages": stage_table(r2, peaks), "mean_accept_len": r2["tau"],
+                     "clocks": r2["clocks"]})
+        del r2
     if rank != 0:
         if world > 1:
             tdist.destroy_process_group()
@@ -668,7 +676,7 @@ def main(argv=None):
         "launches_per_step": n_launch,
         "clocks": res["clocks"],
         "mean_accept_len": res["tau"],
-        "also": also,
+        "also": also or None,
         "next_rows": res["next_rows"],
     }
     print(json.dumps(line), flush=True)
