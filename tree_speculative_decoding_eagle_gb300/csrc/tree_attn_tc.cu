@@ -14,18 +14,18 @@
 //   * producer warp: K/V tiles into a ring of shared-memory stages, by TMA
 //     (128-byte swizzle) for full tiles, by plain loads with zero fill for
 //     the ragged last prefix tile;
-//   * MMA warp (one elected thread): S_t = Q_t K^T (A = Q from shared
-//     memory) and O_t += P_t V (A = P from tensor memory), accumulators in
-//     tensor memory, completion via tcgen05.commit on mbarriers.  Each M-tile
-//     advances on its own events: as soon as its softmax has read S of tile
-//     j, S of tile j+1 is issued for it, then its P.V of tile j;
+//   * MMA warp (one thread): S_t = Q_t K^T (A = Q from shared memory) and
+//     O_t += P_t V (A = P from tensor memory), accumulators in tensor memory,
+//     completion via tcgen05.commit on mbarriers.  Per tile j: S of tile j+1
+//     for every M-tile as soon as its softmax has taken S(j) into registers,
+//     then P(j).V for every M-tile once P(j) is in tensor memory;
 //   * one softmax warpgroup per M-tile: reads its S rows from tensor memory
-//     (a max pass, then an exponent pass), writes P as packed bf16 pairs into
-//     tensor memory, keeps the row sum, and rescales its O rows in tensor
-//     memory only when the running maximum grows by more than 2^8.  With two
-//     M-tiles the exponent passes take turns (a token passed through two
-//     mbarriers), so one M-tile's exponents overlap the other's MMAs and max
-//     pass instead of both competing for the same issue slots.
+//     into registers once and releases S at once (so the next tile's
+//     S = Q K^T runs while this tile's exponents are taken), takes the row
+//     maximum and the exponents, writes P as packed bf16 pairs into tensor
+//     memory, keeps the row sum, and rescales its O rows in tensor memory
+//     only when the running maximum grows by more than 2^8.  A warp whose 32
+//     rows all lie past the last (node, head) row only signals.
 // Tensor memory per M-tile: S (NK columns), P (NK/2), O (dh).
 // KV split (few heads: S <= 8 CTAs share one (b, g, M-group)): the S CTAs
 // are one thread-block cluster; each leaves its unnormalised O and (m, l)
@@ -73,7 +73,7 @@ struct TcShape {
   static constexpr int kTileBytes = kRegions * NK * 128;     // one K (or V) tile
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kBarOff = kQBytes + STAGES * kStageBytes;
-  static constexpr int kNumBars = 2 * STAGES + 4 * MT + 6;
+  static constexpr int kNumBars = 2 * STAGES + 4 * MT + 4;
   static constexpr int kBarBytes = kNumBars * 8 + 16;
   // QR = 128: buffers at the first 1 KB boundary, barriers after them.
   // QR = 64: the barriers sit in the gap before the 1 KB-aligned buffers
@@ -126,8 +126,7 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
   uint64_t *p_full = s_free + MT;
   uint64_t *o_done = p_full + MT;
   uint64_t *teardown = o_done + MT;
-  uint64_t *turn = teardown + 1;  // exponent-pass token of M-tile 0 / 1
-  uint64_t *q_full = turn + 2;    // the Q tiles (TMA)
+  uint64_t *q_full = teardown + 1;  // the Q tiles (TMA)
   uint64_t *cl_full = q_full + 1; // split merge: every CTA of the cluster has its partials in shared memory
   uint64_t *cl_done = cl_full + 1;  // split merge: every CTA of the cluster has read its peers
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Sh::kNumBars);
@@ -180,8 +179,6 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
       mbar_init(&o_done[t], 1);
     }
     mbar_init(teardown, 1);
-    mbar_init(&turn[0], 4);
-    mbar_init(&turn[1], 4);
     mbar_init(q_full, 1);
     if constexpr (SPLIT) {
       mbar_init(cl_full, a.S);
@@ -300,17 +297,23 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
     }
   } else if (warp == mma_warp) {
     // --------------------------------------------------------------------- MMA
+    // Lane 0 issues every MMA and commit.  Shared-memory descriptors advance
+    // by constants from per-stage bases: the start-address field holds the
+    // byte address / 16 and never carries (shared memory is below 256 KB).
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(128, NK, false);
       constexpr uint32_t id_o = idesc_bf16(128, DH, true);
+      const uint64_t q_desc0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t k_desc0 = sdesc_sw128(smem_u32(sKV), 16, 1024);
+      const uint64_t v_desc0 = sdesc_sw128(smem_u32(sKV) + Sh::kTileBytes, NK * 128, 1024);
       auto issue_s = [&](int j, int t) {
-        const uint32_t kaddr = smem_u32(sKV + (j % STAGES) * Sh::kStageBytes);
-        const uint32_t qaddr = smem_u32(sQ + t * Sh::kRegions * Sh::kQRegionBytes);
+        const uint64_t kd = k_desc0 + static_cast<uint64_t>((j % STAGES) * (Sh::kStageBytes >> 4));
+        const uint64_t qd = q_desc0 + static_cast<uint64_t>(t * Sh::kRegions * (Sh::kQRegionBytes >> 4));
 #pragma unroll
         for (int s = 0; s < DH / 16; ++s) {
-          const uint64_t ad = sdesc_sw128(qaddr + (s / 4) * Sh::kQRegionBytes + (s % 4) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(kaddr + (s / 4) * (NK * 128) + (s % 4) * 32, 16, 1024);
-          mma_bf16_ss(tmem + Sh::kColS + t * NK, ad, bd, id_s, s > 0);
+          const uint64_t qoff = static_cast<uint64_t>(((s / 4) * Sh::kQRegionBytes + (s % 4) * 32) >> 4);
+          const uint64_t koff = static_cast<uint64_t>(((s / 4) * (NK * 128) + (s % 4) * 32) >> 4);
+          mma_bf16_ss(tmem + Sh::kColS + t * NK, qd + qoff, kd + koff, id_s, s > 0);
         }
         mma_commit(&s_full[t]);
       };
@@ -319,27 +322,27 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
         tc_fence_after();
         for (int t = 0; t < MT; ++t) issue_s(0, t);
       }
-      // per tile j and M-tile t: S(j+1) as soon as the softmax has read S(j),
-      // then P(j).V once P(j) is in tensor memory
+      // per tile j: S(j+1) of every M-tile as soon as its softmax has taken
+      // S(j) into registers, then P(j).V of every M-tile once P(j) is in
+      // tensor memory
       for (int j = 0; j < T && ok; ++j) {
         const int st = j % STAGES;
         const bool next = j + 1 < T;
         if (next && !mbar_wait(&kv_full[(j + 1) % STAGES], ((j + 1) / STAGES) & 1, abort_flag)) break;
-        const uint32_t vaddr = smem_u32(sKV + st * Sh::kStageBytes) + Sh::kTileBytes;
+        const uint64_t vd = v_desc0 + static_cast<uint64_t>(st * (Sh::kStageBytes >> 4));
+        for (int t = 0; t < MT && ok && next; ++t) {
+          if (!mbar_wait(&s_free[t], j & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(j + 1, t);
+        }
         for (int t = 0; t < MT && ok; ++t) {
-          if (next) {
-            if (!mbar_wait(&s_free[t], j & 1, abort_flag)) { ok = false; break; }
-            tc_fence_after();
-            issue_s(j + 1, t);
-          }
           if (!mbar_wait(&p_full[t], j & 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint32_t pcol = tmem + Sh::kColP + t * (NK / 2);
 #pragma unroll
-          for (int s = 0; s < NK / 16; ++s) {
-            const uint64_t bd = sdesc_sw128(vaddr + s * 2048, NK * 128, 1024);
-            mma_bf16_ts(tmem + Sh::kColO + t * DH, pcol + s * 8, bd, id_o, (j > 0 || s > 0));
-          }
+          for (int s = 0; s < NK / 16; ++s)
+            mma_bf16_ts(tmem + Sh::kColO + t * DH, pcol + s * 8, vd + static_cast<uint64_t>(s * (2048 >> 4)), id_o,
+                        (j > 0 || s > 0));
           mma_commit(&o_done[t]);
         }
         if (ok) mma_commit(&kv_empty[st]);
@@ -351,6 +354,7 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
     const int r = qtr * 32 + lane;
     const int rho = (mg * MT + t) * 128 + r;
     const bool row_ok = rho < rows_total;
+    const bool warp_live = (mg * MT + t) * 128 + qtr * 32 < rows_total;  // warp-uniform
     const int i = row_ok ? rho / a.G : 0;
     const int hh = row_ok ? rho % a.G : 0;
     const uint32_t lane_base = static_cast<uint32_t>(qtr * 32) << 16;
@@ -384,14 +388,6 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
 #pragma unroll
       for (int h = 0; h < NH; ++h) dense = dense && keep[h] == ~0ull;
       dense = __all_sync(0xffffffffu, dense);
-      // scores of one 64-key half, masked keys at -inf
-      auto load_half = [&](int h, float (&sv)[64]) {
-        tmem_ld64(tS + 64 * h, sv);
-        if (!dense) {
-#pragma unroll
-          for (int c = 0; c < 64; ++c) sv[c] = ((keep[h] >> c) & 1ull) ? sv[c] : -INFINITY;
-        }
-      };
       auto half_max = [](const float (&sv)[64]) {
         float mx[4] = {sv[0], sv[1], sv[2], sv[3]};
 #pragma unroll
@@ -403,19 +399,27 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
         }
         return fmax3(fmax3(mx[0], mx[1], mx[2]), mx[3], -INFINITY);
       };
-      // pass 1: masked maximum of the row's scores (a one-half tile keeps its
-      // scores in registers for pass 2)
-      float sv0[64];
+      // S into registers in one read; S's tensor memory is then released, so
+      // the next tile's S = Q K^T runs while this tile's exponents are taken.
+      // A warp whose 32 rows all lie past the last (node, head) row only
+      // signals (its rows' results are never written out).
+      float sv[NH][64];
+      if (warp_live) {
+#pragma unroll
+        for (int h = 0; h < NH; ++h) tmem_ld64(tS + 64 * h, sv[h]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[t]);  // S has been read
       float tmax = -INFINITY;
-      if constexpr (NH == 1) {
-        load_half(0, sv0);
-        tmax = half_max(sv0);
-      } else {
+      if (warp_live) {
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
-          float sv[64];
-          load_half(h, sv);
-          tmax = fmaxf(tmax, half_max(sv));
+          if (!dense) {  // masked keys at -inf
+#pragma unroll
+            for (int c = 0; c < 64; ++c) sv[h][c] = ((keep[h] >> c) & 1ull) ? sv[h][c] : -INFINITY;
+          }
+          tmax = fmaxf(tmax, half_max(sv[h]));
         }
       }
       tmax *= a.scale_log2;  // scale > 0
@@ -427,20 +431,14 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
         if (!warp_wait(&o_done[t], (j - 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
       }
-      if constexpr (MT == 2) {  // wait for this M-tile's turn at the exponent pass
-        if ((t == 1 || j > 0) && !warp_wait(&turn[t], t == 1 ? (j & 1) : ((j - 1) & 1), abort_flag)) {
-          ok = false;
-          break;
-        }
-      }
-      // pass 2: P = exp2(s*scale - base), packed bf16 pairs into tensor memory
-      // (a row with no valid key yet has base -inf and only -inf scores: any
-      // finite exponent base then gives 0)
+      // P = exp2(s*scale - base), packed bf16 pairs into tensor memory (a row
+      // with no valid key yet has base -inf and only -inf scores: any finite
+      // exponent base then gives 0)
       const float nb = base > -INFINITY ? -base : 0.f;
       const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2), nb2 = f2_pack(nb, nb);
       uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
-      // packed P in two 16-column pieces, so only one piece's registers are
-      // live next to the scores
+      // packed P in 16-column pieces, so only one piece's registers are live
+      // next to the scores
       auto exp_half = [&](int h, const float (&sv)[64]) {
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
@@ -458,29 +456,17 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
           }
           tmem_st16_async(tP + 32 * h + 16 * q, pk);
         }
-        tmem_wait_st();
       };
-      if constexpr (NH == 1) {
-        exp_half(0, sv0);
-      } else {
+      if (warp_live) {
 #pragma unroll
-        for (int h = 0; h < NH; ++h) {
-          float sv[64];
-          load_half(h, sv);
-          exp_half(h, sv);
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&s_free[t]);                           // S has been read
-        if constexpr (MT == 2) mbar_arrive(&turn[1 - t]);  // the other M-tile's turn
+        for (int h = 0; h < NH; ++h) exp_half(h, sv[h]);
+        tmem_wait_st();
       }
       float q0, q1, q2, q3;
       f2_unpack(acc0, q0, q1);
       f2_unpack(acc1, q2, q3);
       l = l * alpha + ((q0 + q1) + (q2 + q3));
-      if (j > 0 && __any_sync(0xffffffffu, raise)) {
+      if (warp_live && j > 0 && __any_sync(0xffffffffu, raise)) {
 #pragma unroll
         for (int c0 = 0; c0 < DH; c0 += 32) {
           float o[32];
