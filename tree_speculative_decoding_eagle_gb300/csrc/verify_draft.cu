@@ -22,6 +22,7 @@
 namespace eagle {
 
 constexpr int kVDThreads = 512;
+constexpr int kBatch = 4;  // vectors per thread whose loads are in flight together
 
 struct DraftVerifyArgs {
   const void *target, *draft;
@@ -115,11 +116,25 @@ __global__ void __launch_bounds__(kVDThreads) verify_draft_kernel(DraftVerifyArg
       }
       qrow = reinterpret_cast<const T *>(a.draft) + (static_cast<int64_t>(b) * a.D * a.k + r) * a.ld_d;
     }
-    // (max, sum) of p and q in base-2 units: y = x * inv_t * log2(e)
+    // (max, sum) of p and q in base-2 units: y = x * inv_t * log2(e); each
+    // thread's vectors of a batch are loaded before any is used, so a pass
+    // costs one memory latency per batch, not one per vector
     float mp = -INFINITY, sp = 0.f, mq = -INFINITY, sq = 0.f;
-    for (int vi = tid; vi < nvec; vi += blockDim.x) {
+    for (int base = 0; base < nvec; base += kBatch * kVDThreads) {
+      uint4 bp[kBatch], bq[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int vi = base + k * kVDThreads + tid;
+        if (vi < nvec) {
+          bp[k] = *reinterpret_cast<const uint4 *>(prow + static_cast<int64_t>(vi) * VEC);
+          if (qrow) bq[k] = *reinterpret_cast<const uint4 *>(qrow + static_cast<int64_t>(vi) * VEC);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+      if (base + k * kVDThreads + tid >= nvec) continue;
       float x[VEC];
-      VT::unpack(*reinterpret_cast<const uint4 *>(prow + static_cast<int64_t>(vi) * VEC), x);
+      VT::unpack(bp[k], x);
       float vm = x[0];
 #pragma unroll
       for (int e = 1; e < VEC; ++e) vm = fmaxf(vm, x[e]);
@@ -133,7 +148,7 @@ __global__ void __launch_bounds__(kVDThreads) verify_draft_kernel(DraftVerifyArg
         mp = mn;
       }
       if (qrow) {
-        VT::unpack(*reinterpret_cast<const uint4 *>(qrow + static_cast<int64_t>(vi) * VEC), x);
+        VT::unpack(bq[k], x);
         float wm = x[0];
 #pragma unroll
         for (int e = 1; e < VEC; ++e) wm = fmaxf(wm, x[e]);
@@ -146,6 +161,7 @@ __global__ void __launch_bounds__(kVDThreads) verify_draft_kernel(DraftVerifyArg
           sq = (mq == -INFINITY ? 0.f : sq * ex2_approx(mq - mq2)) + acc_q;
           mq = mq2;
         }
+      }
       }
     }
     // lse_combine works in natural units: convert, merge, convert back
@@ -182,13 +198,26 @@ __global__ void __launch_bounds__(kVDThreads) verify_draft_kernel(DraftVerifyArg
       }
       C += S;
       float part = 0.f;
-      for (int vi = tid; vi < nvec; vi += blockDim.x) {
-        float xp[VEC], xq[VEC];
-        VT::unpack(*reinterpret_cast<const uint4 *>(prow + static_cast<int64_t>(vi) * VEC), xp);
-        VT::unpack(*reinterpret_cast<const uint4 *>(qrow + static_cast<int64_t>(vi) * VEC), xq);
+      for (int base = 0; base < nvec; base += kBatch * kVDThreads) {
+        uint4 bp[kBatch], bq[kBatch];
 #pragma unroll
-        for (int e = 0; e < VEC; ++e)
-          part += fmaxf(0.f, ex2_approx(fmaf(xp[e], sc, -mp)) * ip - C * ex2_approx(fmaf(xq[e], sc, -mq)) * iq);
+        for (int k = 0; k < kBatch; ++k) {
+          const int vi = base + k * kVDThreads + tid;
+          if (vi < nvec) {
+            bp[k] = *reinterpret_cast<const uint4 *>(prow + static_cast<int64_t>(vi) * VEC);
+            bq[k] = *reinterpret_cast<const uint4 *>(qrow + static_cast<int64_t>(vi) * VEC);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+          if (base + k * kVDThreads + tid >= nvec) continue;
+          float xp[VEC], xq[VEC];
+          VT::unpack(bp[k], xp);
+          VT::unpack(bq[k], xq);
+#pragma unroll
+          for (int e = 0; e < VEC; ++e)
+            part += fmaxf(0.f, ex2_approx(fmaf(xp[e], sc, -mp)) * ip - C * ex2_approx(fmaf(xq[e], sc, -mq)) * iq);
+        }
       }
       S = block_sum(part, s_red);
       if (!(S > 0.f)) {  // nothing left: fall back to p
@@ -210,14 +239,27 @@ __global__ void __launch_bounds__(kVDThreads) verify_draft_kernel(DraftVerifyArg
     const int per = (nvec + blockDim.x - 1) / blockDim.x;
     const int v0 = min(nvec, tid * per), v1 = min(nvec, v0 + per);
     float own = 0.f;
-    for (int vi = v0; vi < v1; ++vi) {
-      float xp[VEC], xq[VEC];
-      VT::unpack(*reinterpret_cast<const uint4 *>(prow + static_cast<int64_t>(vi) * VEC), xp);
-      if (qrow && C > 0.f) VT::unpack(*reinterpret_cast<const uint4 *>(qrow + static_cast<int64_t>(vi) * VEC), xq);
+    const bool use_q = qrow && C > 0.f;
+    for (int vb = v0; vb < v1; vb += kBatch) {
+      uint4 bp[kBatch], bq[kBatch];
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        const float p = ex2_approx(fmaf(xp[e], sc, -mp)) * ip;
-        own += (qrow && C > 0.f) ? fmaxf(0.f, p - C * ex2_approx(fmaf(xq[e], sc, -mq)) * iq) : p;
+      for (int k = 0; k < kBatch; ++k) {
+        if (vb + k < v1) {
+          bp[k] = *reinterpret_cast<const uint4 *>(prow + static_cast<int64_t>(vb + k) * VEC);
+          if (use_q) bq[k] = *reinterpret_cast<const uint4 *>(qrow + static_cast<int64_t>(vb + k) * VEC);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        if (vb + k >= v1) continue;
+        float xp[VEC], xq[VEC];
+        VT::unpack(bp[k], xp);
+        if (use_q) VT::unpack(bq[k], xq);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          const float p = ex2_approx(fmaf(xp[e], sc, -mp)) * ip;
+          own += use_q ? fmaxf(0.f, p - C * ex2_approx(fmaf(xq[e], sc, -mq)) * iq) : p;
+        }
       }
     }
     // exclusive block scan of `own`
