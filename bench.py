@@ -304,8 +304,7 @@ def measure_next_rows(step, sets, w, work, peaks):
     out["kv_commit"] = {"ms": round(per_launch_ms(run_commit), 5), "accepted": int(step.accept_len.sum().item())}
     out["kv_commit"]["status"] = int(status.item())
     # f2: speculative-sampling verification against the draft distributions
-    n = w.m + 1
-    u = torch.rand((w.B, n, 2), device=kvl.device)
+    u = torch.from_numpy(gen.uniforms(w)).to(kvl.device)  # the workload's seeded Philox uniforms
 
     def run_vd(i):
         s_ = sets[i % copies]

@@ -41,7 +41,7 @@ cudaError_t launch_static_tree(const int32_t *tok, const float *conf, int B, int
                                const int32_t *rank, int n, const int32_t *root_tok, int32_t *node_tok,
                                int32_t *node_parent, int32_t *node_depth, float *node_score, int32_t *node_src,
                                int32_t *node_row, uint64_t *mask, int32_t *status, cudaStream_t st);
-size_t tree_smem_bytes(int D, int k, int m);
+size_t tree_smem_bytes(int D, int k, int m, int flags);
 // tree_attn_simt.cu / tree_attn_tc.cu
 size_t attn_simt_workspace_bytes(int B, int n, int Hq, int dh, int Lmax, int num_sms);
 cudaError_t launch_tree_attn_simt(const void *q, const void *k_cache, const void *v_cache,
@@ -134,7 +134,7 @@ int eagle_tree_build_variant(const int32_t *tok, const float *conf, int B, int D
   const int64_t NC = k + static_cast<int64_t>(D - 1) * k * k;
   if (NC > 4095 || m > NC) return EAGLE_ERR_INVALID;
   if ((flags & EAGLE_TREE_NO_RERANK) && m > static_cast<int64_t>(D) * k) return EAGLE_ERR_INVALID;
-  if (tree_smem_bytes(D, k, m) > 227 * 1024) return EAGLE_ERR_UNSUPPORTED;  // one CTA's shared memory
+  if (tree_smem_bytes(D, k, m, flags) > 227 * 1024) return EAGLE_ERR_UNSUPPORTED;  // one CTA's shared memory
   return from_cuda(launch_tree_build(tok, conf, B, D, k, m, flags, root_tok, node_tok, node_parent,
                                      node_depth, node_score, node_src, node_row, mask, status,
                                      reinterpret_cast<cudaStream_t>(stream)));

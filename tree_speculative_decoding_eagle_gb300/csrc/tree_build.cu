@@ -102,6 +102,8 @@ __global__ void __launch_bounds__(kTreeThreads) tree_build_kernel(TreeArgs a) {
   int *s_E = s_sel + m;                                          // [k] expanded gids by rank
   int *s_tok = s_E + k;                                          // [R*k] used rows
   float *s_conf = reinterpret_cast<float *>(s_tok + R * k);
+  // confidence only: group e's children sorted by key, [R][k] gids
+  int *s_gs = reinterpret_cast<int *>(s_conf + R * k);
   __shared__ int s_bad;
   const bool conf_only = (a.flags & EAGLE_TREE_CONFIDENCE_ONLY) != 0;
   const bool rerank = (a.flags & EAGLE_TREE_NO_RERANK) == 0;
@@ -223,10 +225,86 @@ __global__ void __launch_bounds__(kTreeThreads) tree_build_kernel(TreeArgs a) {
 
   // ---- selection in output order ----------------------------------------
   const int *sel = full ? (s_Lg + cur * m) : s_sel;
-  if (!full && rerank) {
+  if (!full && rerank && R <= 64) {
     // confidence only: best-first growth, m picks of the greatest key whose
-    // parent is already in the tree (s_out >= 0); each pick is a block-wide
-    // arg-max (thread scan, warp shuffles, then the warps' winners)
+    // parent is already in the tree.  The open candidates are the children
+    // of the nodes already picked, one group per expanded node (group e: the
+    // root's children for e = 0, else those of E_d[j] for e = 1+(d-1)k+j,
+    // gids consecutive by child rank).  One warp holds every group's best
+    // remaining child (lane e % 32, slot e / 32): a pick is the warp maximum
+    // of those heads (two 32-bit reductions), the winner's group then finds
+    // its next head, and a picked node that was expanded opens its group.
+    auto first_child = [&](int e) {
+      return e == 0 ? 1 : layer_base(2 + (e - 1) / k, k) + ((e - 1) % k) * k;
+    };
+    // every group's children sorted by key (rank = siblings with a greater
+    // key); slots start at a valid gid, so keys that collide (a row that
+    // repeats a token, outside the domain) leave nothing out of range
+    for (int q = tid; q < R * k; q += blockDim.x) s_gs[q] = first_child(q / k) + q % k;
+    __syncthreads();
+    for (int q = tid; q < R * k; q += blockDim.x) {
+      const int e = q / k, g0 = first_child(e), g = g0 + q % k;
+      const uint64_t key = s_key[g];
+      int pos = 0;
+      for (int r = 0; r < k; ++r) pos += s_key[g0 + r] > key;
+      s_gs[e * k + pos] = g;
+    }
+    __syncthreads();
+    if (tid < 32) {
+      const int lane = tid;
+      // lane l holds groups l (slot 0) and l + 32 (slot 1): children taken
+      // so far (the next head is the child of that rank) and the head
+      int n0 = 0, n1 = 0;
+      uint64_t hk0 = 0, hk1 = 0;
+      int hg0 = -1, hg1 = -1;
+      auto head = [&](int e, int taken, uint64_t &hk, int &hg) {
+        hg = taken < k ? s_gs[e * k + taken] : -1;
+        hk = hg >= 0 ? s_key[hg] : 0ull;
+      };
+      if (lane == 0) head(0, 0, hk0, hg0);  // the root's group is open
+      for (int pick = 0; pick < m; ++pick) {
+        const bool use1 = hg1 >= 0 && (hg0 < 0 || hk1 > hk0);
+        const uint64_t bk = use1 ? hk1 : hk0;
+        const int bg = use1 ? hg1 : hg0;
+        const bool has = bg >= 0;
+        const uint32_t hi = static_cast<uint32_t>(bk >> 32), lo = static_cast<uint32_t>(bk);
+        const uint32_t mhi = __reduce_max_sync(0xffffffffu, has ? hi : 0u);
+        const bool c1 = has && hi == mhi;
+        const uint32_t mlo = __reduce_max_sync(0xffffffffu, c1 ? lo : 0u);
+        const unsigned win = __ballot_sync(0xffffffffu, c1 && lo == mlo);
+        if (!win) {  // nothing left to add (cannot happen for m <= candidates)
+          if (lane == 0) {
+            s_bad = 1;
+            for (int q = pick; q < m; ++q) s_sel[q] = 0;
+          }
+          break;
+        }
+        const int wl = __ffs(win) - 1;
+        const int g = __shfl_sync(0xffffffffu, bg, wl);
+        if (lane == 0) {
+          s_sel[pick] = g;
+          s_out[g] = pick + 1;
+        }
+        if (lane == wl) {  // the winner's group moves to its next child
+          if (use1) head(lane + 32, ++n1, hk1, hg1);
+          else head(lane, ++n0, hk0, hg0);
+        }
+        // a picked node that was expanded (row d*k + j, d >= 1) opens group 1 + row - k
+        const int row = s_row[g];
+        if (row >= k) {
+          const int e = 1 + row - k;
+          if (lane == (e & 31)) {
+            if (e >= 32) head(e, 0, hk1, hg1);
+            else head(e, 0, hk0, hg0);
+          }
+        }
+      }
+    }
+  } else if (!full && rerank) {
+    // confidence only with more than 64 expanded nodes: each pick is a
+    // block-wide arg-max over every candidate whose parent is already in
+    // the tree (s_out >= 0): thread scan, warp shuffles, then the warps'
+    // winners
     __shared__ uint64_t s_wbest[kTreeThreads / 32];
     __shared__ int s_wg[kTreeThreads / 32];
     const int lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
@@ -353,7 +431,7 @@ __global__ void __launch_bounds__(256) tree_mask_kernel(const int32_t *parent, i
 
 // ---- host side ---------------------------------------------------------------
 
-size_t tree_smem_bytes(int D, int k, int m) {
+size_t tree_smem_bytes(int D, int k, int m, int flags) {
   const int NC = k + (D - 1) * k * k;
   const int kk = k * k;
   size_t bytes = sizeof(uint64_t) * (NC + 1)          // s_key
@@ -362,7 +440,8 @@ size_t tree_smem_bytes(int D, int k, int m) {
                + sizeof(int) * (2 * kk + m)           // s_cnt
                + sizeof(int) * 2 * (NC + 1)           // s_row, s_out
                + sizeof(int) * m + sizeof(int) * k    // s_sel, s_E
-               + 8 * static_cast<size_t>(1 + (D - 1) * k) * k;  // s_tok, s_conf
+               + 8 * static_cast<size_t>(1 + (D - 1) * k) * k  // s_tok, s_conf
+               + ((flags & EAGLE_TREE_CONFIDENCE_ONLY) ? 4 * static_cast<size_t>(1 + (D - 1) * k) * k : 0);  // s_gs
   return (bytes + 15) / 16 * 16;
 }
 
@@ -378,7 +457,7 @@ cudaError_t launch_tree_build(const int32_t *tok, const float *conf, int B, int 
   a.node_tok = node_tok; a.node_parent = node_parent; a.node_depth = node_depth;
   a.node_src = node_src; a.node_row = node_row; a.node_score = node_score;
   a.mask = mask; a.status = status;
-  const size_t smem = tree_smem_bytes(D, k, m);
+  const size_t smem = tree_smem_bytes(D, k, m, flags);
   if (smem > 48 * 1024) {
     // the limit is raised once per device to the opt-in maximum, so it only
     // ever grows (two host threads with different sizes cannot undo each other)
