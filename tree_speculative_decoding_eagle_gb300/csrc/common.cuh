@@ -57,6 +57,7 @@ template <> struct VecTraits<float> {
     x[0] = __uint_as_float(v.x); x[1] = __uint_as_float(v.y);
     x[2] = __uint_as_float(v.z); x[3] = __uint_as_float(v.w);
   }
+  __device__ __forceinline__ static uint4 neg_inf_vec() { return make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u); }
   __device__ __forceinline__ static float load1(const void *p, int64_t i) {
     return __ldg(reinterpret_cast<const float *>(p) + i);
   }
@@ -67,6 +68,7 @@ template <> struct VecTraits<__nv_bfloat16> {
     x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
     x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z); x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
   }
+  __device__ __forceinline__ static uint4 neg_inf_vec() { return make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u); }
   __device__ __forceinline__ static float load1(const void *p, int64_t i) {
     const unsigned short *s = reinterpret_cast<const unsigned short *>(p);
     return __uint_as_float(static_cast<uint32_t>(__ldg(s + i)) << 16);

@@ -22,7 +22,7 @@
 // (shared block-wide as a maximum over the warps) are never looked at;
 // before the list is full, the k-th largest lane maximum is the bound.  In
 // the ring form the lanes also keep their running maxima in shared memory,
-// and every fourth segment a warp raises the shared bound to the k-th
+// and every eighth segment a warp raises the shared bound to the k-th
 // largest of their group maxima (distinct elements, so a valid bound
 // whenever read): the bound then reflects the whole block's progress
 // rather than one warp's share of the row.  The warp lists
@@ -108,15 +108,16 @@ template <> __device__ __forceinline__ float elem_of<float>(const uint4 &v, int 
 
 // Sum over a lane's vectors of 2^(x log2e + nmL): even and odd elements in
 // the two halves of a packed pair, one FMA and one add for every two
-// elements (each half rounds exactly as its scalar form).
-template <typename T, int NVL>
+// elements (each half rounds exactly as its scalar form).  kAll: every
+// vector holds data (missing ones are -inf padding), so none is skipped.
+template <typename T, int NVL, bool kAll = false>
 __device__ __forceinline__ float segment_exp_sum(const uint4 (&vb)[NVL], int nvec, int lane, float nmL) {
   constexpr int VEC = VecTraits<T>::kElems;
   const uint64_t c2 = f2_pack(kLog2e, kLog2e), n2 = f2_pack(nmL, nmL);
   uint64_t acc = f2_pack(0.f, 0.f);
 #pragma unroll
   for (int i = 0; i < NVL; ++i) {
-    if (lane + 32 * i < nvec) {
+    if (kAll || lane + 32 * i < nvec) {
       float x[VEC];
       VecTraits<T>::unpack(vb[i], x);
 #pragma unroll
@@ -179,15 +180,26 @@ __global__ void __launch_bounds__(NW * 32, NW <= 8 ? 3 : 1) draft_topk_kernel(Dr
   constexpr int kStages = 3;
   extern __shared__ __align__(16) uint4 s_ring[];
   uint4 *my_ring = s_ring + warp * kStages * NVL * 32;
+  // A full segment takes NVL unconditional copies at constant offsets; in
+  // the row's last, partial segment a lane writes -inf padding into the
+  // slots past the row's end (it alone reads them back), so every later
+  // step handles all NVL vectors alike: -inf adds nothing to a maximum, an
+  // exponential sum or a top-k list.
   auto issue_segment = [&](int gseg, int stage) {
     if (gseg < g1) {
       const int seg0 = gseg * SEG;
-      const int nvec = min(SEG, a.V - seg0) / VEC;
-      uint4 *dst = my_ring + stage * NVL * 32;
+      const T *src = row + seg0 + lane * VEC;
+      uint4 *dst = my_ring + stage * NVL * 32 + lane;
+      if (seg0 + SEG <= a.V) {
 #pragma unroll
-      for (int i = 0; i < NVL; ++i) {
-        const int v = lane + 32 * i;
-        if (v < nvec) cp_async16(dst + v, row + seg0 + v * VEC);
+        for (int i = 0; i < NVL; ++i) cp_async16(dst + 32 * i, src + 32 * i * VEC);
+      } else {
+        const int nvec = (a.V - seg0) / VEC;
+#pragma unroll
+        for (int i = 0; i < NVL; ++i) {
+          if (lane + 32 * i < nvec) cp_async16(dst + 32 * i, src + 32 * i * VEC);
+          else dst[32 * i] = VT::neg_inf_vec();
+        }
       }
     }
     cp_async_commit();
@@ -360,38 +372,38 @@ __global__ void __launch_bounds__(NW * 32, NW <= 8 ? 3 : 1) draft_topk_kernel(Dr
     }
     __syncthreads();
   } else {
+    static_assert(kRing, "the streaming form is the shared-memory ring");
+    int st_read = 0, st_issue = kStages - 1;  // ring stages, advanced without division
     for (int gseg = g0 + warp, it = 0; gseg < g1; gseg += NW, ++it) {
       const int seg0 = gseg * SEG;
-      const int nvec = min(SEG, a.V - seg0) / VEC;
-      if constexpr (kRing) {
-        // the stage read one iteration ago takes the segment kStages-1 ahead;
-        // this iteration's copies are then complete
-        issue_segment(gseg + (kStages - 1) * NW, (it + kStages - 1) % kStages);
-        cp_async_wait<kStages - 1>();
-        const uint4 *src = my_ring + (it % kStages) * NVL * 32;
+      // the stage read one iteration ago takes the segment kStages-1 ahead;
+      // this iteration's copies are then complete
+      issue_segment(gseg + (kStages - 1) * NW, st_issue);
+      st_issue = st_issue == kStages - 1 ? 0 : st_issue + 1;
+      cp_async_wait<kStages - 1>();
+      {
+        const uint4 *src = my_ring + st_read * NVL * 32 + lane;
 #pragma unroll
-        for (int i = 0; i < NVL; ++i)
-          if (lane + 32 * i < nvec) vb[i] = src[lane + 32 * i];
-      } else {
-        if (gseg != g0 + warp) load_segment(gseg);
+        for (int i = 0; i < NVL; ++i) vb[i] = src[32 * i];
       }
+      st_read = st_read == kStages - 1 ? 0 : st_read + 1;
       float smax = -INFINITY;
       float vmx[NVL];
   #pragma unroll
       for (int i = 0; i < NVL; ++i) {
-        vmx[i] = (lane + 32 * i < nvec) ? vec_max<T>(vb[i]) : -INFINITY;
+        vmx[i] = vec_max<T>(vb[i]);
         smax = fmaxf(smax, vmx[i]);
       }
-      if (smax > -INFINITY) lse_combine(m, sum, smax, segment_exp_sum<T, NVL>(vb, nvec, lane, -smax * kLog2e));
+      if (smax > -INFINITY) lse_combine(m, sum, smax, segment_exp_sum<T, NVL, true>(vb, 0, lane, -smax * kLog2e));
       lmax = fmaxf(lmax, smax);
       // block bound from the lanes' running maxima: a slot only ever holds an
       // element of this part (or -inf), whenever it is read, and distinct
       // slots hold distinct elements, so the k-th largest of any slots
-      // bounds the part's k-th largest from below.  Every fourth segment a
+      // bounds the part's k-th largest from below.  Every eighth segment a
       // warp takes the maxima of 32 groups of 8 slots and raises the shared
       // bound to their k-th largest.
       s_lmax[tid] = lmax;
-      if (((it + warp) & 3) == 0) {
+      if (((it + warp) & 7) == 0) {
         float g[8];
         asm volatile("ld.volatile.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
                      : "=f"(g[0]), "=f"(g[1]), "=f"(g[2]), "=f"(g[3]) : "r"(smem_u32(s_lmax + 8 * lane)));
