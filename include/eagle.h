@@ -407,12 +407,14 @@ int eagle_verify_noalloc(const void *target, int dtype, int64_t ld,
  *              every node that has children
  *   uniforms   device float [B, m+1, 2] in [0, 1)
  *   accept_len, path_nodes, out_tokens, status   as in eagle_verify
- * No workspace: one CTA per sequence keeps its state in shared memory.
+ * No workspace: the CTAs of a sequence (one thread-block cluster of up to
+ * 8, each over a slice of the vocabulary) keep their state in shared memory
+ * and exchange their partial sums through distributed shared memory.
  * Device errors: a node with children whose node_row is outside [0, D*k),
  * a token outside [0, V) or no residual mass set EAGLE_ERR_INVALID.
  * Limits: temperature > 0; V*elemsize, ld_t*elemsize and ld_d*elemsize
  * multiples of 16 bytes; 16-byte aligned logits; 1 <= m+1 <= 4096;
- * 1 <= D; 1 <= k <= 32.
+ * 1 <= D; 1 <= k <= 32; B <= 65535 (else EAGLE_ERR_UNSUPPORTED).
  * ------------------------------------------------------------------------ */
 int eagle_verify_draft(const void *target, const void *draft, int dtype,
                        int64_t ld_t, int64_t ld_d, const int32_t *node_tok,

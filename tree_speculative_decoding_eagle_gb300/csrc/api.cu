@@ -287,6 +287,7 @@ int eagle_verify_draft(const void *target, const void *draft, int dtype, int64_t
   if ((static_cast<int64_t>(V) * es) % 16 || (ld_t * es) % 16 || (ld_d * es) % 16 || !aligned16(target) ||
       !aligned16(draft))
     return EAGLE_ERR_INVALID;
+  if (B > 65535) return EAGLE_ERR_UNSUPPORTED;  // sequences index the grid's y dimension
   return from_cuda(launch_verify_draft(target, draft, dtype, ld_t, ld_d, node_tok, node_parent, node_row, B, m,
                                        D, k, V, temperature, uniforms, accept_len, path_nodes, out_tokens, status,
                                        reinterpret_cast<cudaStream_t>(stream)));

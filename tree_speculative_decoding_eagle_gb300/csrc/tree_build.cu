@@ -102,8 +102,9 @@ __global__ void __launch_bounds__(kTreeThreads) tree_build_kernel(TreeArgs a) {
   int *s_E = s_sel + m;                                          // [k] expanded gids by rank
   int *s_tok = s_E + k;                                          // [R*k] used rows
   float *s_conf = reinterpret_cast<float *>(s_tok + R * k);
-  // confidence only: group e's children sorted by key, [R][k] gids
-  int *s_gs = reinterpret_cast<int *>(s_conf + R * k);
+  // confidence only: group e's children sorted by key, [R][k] head values
+  // (see the pick loop), 8-byte aligned
+  uint64_t *s_grec = reinterpret_cast<uint64_t *>((reinterpret_cast<uintptr_t>(s_conf + R * k) + 7) & ~static_cast<uintptr_t>(7));
   __shared__ int s_bad;
   const bool conf_only = (a.flags & EAGLE_TREE_CONFIDENCE_ONLY) != 0;
   const bool rerank = (a.flags & EAGLE_TREE_NO_RERANK) == 0;
@@ -231,73 +232,91 @@ __global__ void __launch_bounds__(kTreeThreads) tree_build_kernel(TreeArgs a) {
     // of the nodes already picked, one group per expanded node (group e: the
     // root's children for e = 0, else those of E_d[j] for e = 1+(d-1)k+j,
     // gids consecutive by child rank).  One warp holds every group's best
-    // remaining child (lane e % 32, slot e / 32): a pick is the warp maximum
-    // of those heads (two 32-bit reductions), the winner's group then finds
-    // its next head, and a picked node that was expanded opens its group.
+    // remaining child (lane e % 32, slot e / 32).  A group's children only
+    // ever compete through their best, and two heads never share a parent,
+    // so among heads the key order is the order of (score, 4095 - parent
+    // gid), and a head is held as the 64-bit value
+    //   score bits:32 | (4095 - parent gid):12 | gid:12 | (opened group + 1):7
+    // (the opened group: the group a pick of this node opens, -1 if none).
+    // A pick is two 32-bit warp maxima (the high word, then the low word
+    // among the lanes that hold that high word), which carry the winner's
+    // gid and opened group; the winner's slot and the opened group's slot
+    // then take their new heads from registers.  No vote, shuffle, branch
+    // or shared-memory load on a pick's critical path.
     auto first_child = [&](int e) {
       return e == 0 ? 1 : layer_base(2 + (e - 1) / k, k) + ((e - 1) % k) * k;
     };
+    auto head_value = [&](int g) {
+      const uint64_t key = s_key[g];
+      const int row = s_row[g];
+      const int opens = row >= k && 1 + row - k < R ? 1 + row - k : -1;
+      const uint32_t lo = (static_cast<uint32_t>(kMaxGid - tkey_parent(key)) << 19) |
+                          (static_cast<uint32_t>(g) << 7) | static_cast<uint32_t>(opens + 1);
+      return (key & 0xFFFFFFFF00000000ull) | lo;
+    };
     // every group's children sorted by key (rank = siblings with a greater
-    // key); slots start at a valid gid, so keys that collide (a row that
-    // repeats a token, outside the domain) leave nothing out of range
-    for (int q = tid; q < R * k; q += blockDim.x) s_gs[q] = first_child(q / k) + q % k;
+    // key); every slot first holds a valid value, so keys that collide (a
+    // row that repeats a token, outside the domain) leave nothing out of range
+    for (int q = tid; q < R * k; q += blockDim.x) s_grec[q] = head_value(first_child(q / k) + q % k);
     __syncthreads();
     for (int q = tid; q < R * k; q += blockDim.x) {
       const int e = q / k, g0 = first_child(e), g = g0 + q % k;
       const uint64_t key = s_key[g];
       int pos = 0;
       for (int r = 0; r < k; ++r) pos += s_key[g0 + r] > key;
-      s_gs[e * k + pos] = g;
+      s_grec[e * k + pos] = head_value(g);
     }
     __syncthreads();
     if (tid < 32) {
       const int lane = tid;
-      // lane l holds groups l (slot 0) and l + 32 (slot 1): children taken
-      // so far (the next head is the child of that rank) and the head
+      // groups lane (slot 0) and lane + 32 (slot 1): the index of the head
+      // child, the head value (0: no head), the group's first child and the
+      // child after the head, both held in registers so that a pick takes
+      // its new head from a register (the load that refills `next` is off
+      // the pick's critical path)
+      const bool ok0 = lane < R, ok1 = lane + 32 < R;
+      const uint64_t first0 = ok0 ? s_grec[lane * k] : 0ull, first1 = ok1 ? s_grec[(lane + 32) * k] : 0ull;
+      uint64_t next0 = ok0 && k > 1 ? s_grec[lane * k + 1] : 0ull;
+      uint64_t next1 = ok1 && k > 1 ? s_grec[(lane + 32) * k + 1] : 0ull;
       int n0 = 0, n1 = 0;
-      uint64_t hk0 = 0, hk1 = 0;
-      int hg0 = -1, hg1 = -1;
-      auto head = [&](int e, int taken, uint64_t &hk, int &hg) {
-        hg = taken < k ? s_gs[e * k + taken] : -1;
-        hk = hg >= 0 ? s_key[hg] : 0ull;
-      };
-      if (lane == 0) head(0, 0, hk0, hg0);  // the root's group is open
+      uint64_t h0 = lane == 0 ? first0 : 0ull, h1 = 0ull;  // the root's group is open
       for (int pick = 0; pick < m; ++pick) {
-        const bool use1 = hg1 >= 0 && (hg0 < 0 || hk1 > hk0);
-        const uint64_t bk = use1 ? hk1 : hk0;
-        const int bg = use1 ? hg1 : hg0;
-        const bool has = bg >= 0;
-        const uint32_t hi = static_cast<uint32_t>(bk >> 32), lo = static_cast<uint32_t>(bk);
-        const uint32_t mhi = __reduce_max_sync(0xffffffffu, has ? hi : 0u);
-        const bool c1 = has && hi == mhi;
-        const uint32_t mlo = __reduce_max_sync(0xffffffffu, c1 ? lo : 0u);
-        const unsigned win = __ballot_sync(0xffffffffu, c1 && lo == mlo);
-        if (!win) {  // nothing left to add (cannot happen for m <= candidates)
-          if (lane == 0) {
-            s_bad = 1;
-            for (int q = pick; q < m; ++q) s_sel[q] = 0;
-          }
-          break;
-        }
-        const int wl = __ffs(win) - 1;
-        const int g = __shfl_sync(0xffffffffu, bg, wl);
+        const uint64_t best = h0 > h1 ? h0 : h1;
+        const uint32_t bhi = static_cast<uint32_t>(best >> 32), blo = static_cast<uint32_t>(best);
+        const uint32_t mhi = __reduce_max_sync(0xffffffffu, bhi);
+        const uint32_t mlo = __reduce_max_sync(0xffffffffu, bhi == mhi ? blo : 0u);
+        // mlo == 0: no head left (cannot happen for m <= candidates, since
+        // every candidate's parent is expanded); flagged, nothing moves
+        const int g = static_cast<int>((mlo >> 7) & 0xFFF);
+        const int e = static_cast<int>(mlo & 127) - 1;
         if (lane == 0) {
           s_sel[pick] = g;
-          s_out[g] = pick + 1;
+          if (g > 0) s_out[g] = pick + 1;
+          else s_bad = 1;
         }
-        if (lane == wl) {  // the winner's group moves to its next child
-          if (use1) head(lane + 32, ++n1, hk1, hg1);
-          else head(lane, ++n0, hk0, hg0);
+        // the winner's group moves to its next child; a picked node that
+        // was expanded opens its group (never the winner's own group)
+        const uint64_t won = (static_cast<uint64_t>(mhi) << 32) | mlo;
+        const bool w0 = mlo != 0 && h0 == won, w1 = mlo != 0 && h1 == won;
+        const bool o0 = ok0 && e == lane, o1 = ok1 && e == lane + 32;
+        if (w0) {
+          h0 = next0;
+          ++n0;
         }
-        // a picked node that was expanded (row d*k + j, d >= 1) opens group 1 + row - k
-        const int row = s_row[g];
-        if (row >= k) {
-          const int e = 1 + row - k;
-          if (lane == (e & 31)) {
-            if (e >= 32) head(e, 0, hk1, hg1);
-            else head(e, 0, hk0, hg0);
-          }
+        if (o0) {
+          h0 = first0;
+          n0 = 0;
         }
+        if (w1) {
+          h1 = next1;
+          ++n1;
+        }
+        if (o1) {
+          h1 = first1;
+          n1 = 0;
+        }
+        if (w0 || o0) next0 = n0 + 1 < k ? s_grec[lane * k + n0 + 1] : 0ull;
+        if (w1 || o1) next1 = n1 + 1 < k ? s_grec[(lane + 32) * k + n1 + 1] : 0ull;
       }
     }
   } else if (!full && rerank) {
@@ -441,7 +460,7 @@ size_t tree_smem_bytes(int D, int k, int m, int flags) {
                + sizeof(int) * 2 * (NC + 1)           // s_row, s_out
                + sizeof(int) * m + sizeof(int) * k    // s_sel, s_E
                + 8 * static_cast<size_t>(1 + (D - 1) * k) * k  // s_tok, s_conf
-               + ((flags & EAGLE_TREE_CONFIDENCE_ONLY) ? 4 * static_cast<size_t>(1 + (D - 1) * k) * k : 0);  // s_gs
+               + ((flags & EAGLE_TREE_CONFIDENCE_ONLY) ? 8 + 8 * static_cast<size_t>(1 + (D - 1) * k) * k : 0);  // s_grec
   return (bytes + 15) / 16 * 16;
 }
 
