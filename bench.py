@@ -431,26 +431,51 @@ def bench_workload(w, args, rank, world, device, with_e2e, next_rows=False):
 def bench_e2e(step, base, graph, dev_set, args, world, device):
     """Same step through the public API with host buffers: every step copies
     its inputs from pinned host memory, calls TreeStep (one C-ABI call per
-    stage) and reads its result back.  `graph_value` replays the same calls
-    captured in a CUDA graph instead (how a serving loop would issue them)."""
+    stage) and reads its result back.  The inputs sit in one pinned staging
+    buffer (each at a 256-byte aligned offset) and arrive in one copy into one
+    device buffer that the step reads through views: one large copy moves
+    faster than one per tensor.  `graph_value` replays the same calls captured
+    in a CUDA graph instead (how a serving loop would issue them)."""
     import torch
     import torch.distributed as tdist
     from tree_speculative_decoding_eagle_gb300.replicas import max_over_ranks
-    host = {k: (v.cpu().pin_memory() if v is not None else None) for k, v in dev_set.items()}
-    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+    names = [k for k, v in dev_set.items() if v is not None]
+    offs, off = {}, 0
+    for k in names:
+        off = (off + 255) // 256 * 256
+        offs[k] = off
+        off += dev_set[k].numel() * dev_set[k].element_size()
+    total = (off + 255) // 256 * 256
+    host_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
+    dev_buf = torch.empty(total, dtype=torch.uint8, device=device)
+
+    def view(buf, k):
+        v = dev_set[k]
+        nb = v.numel() * v.element_size()
+        return buf[offs[k]:offs[k] + nb].view(v.dtype).view(v.shape)
+
+    for k in names:
+        view(host_buf, k).copy_(dev_set[k].cpu())
+    packed = {k: (view(dev_buf, k) if v is not None else None) for k, v in dev_set.items()}
+    dev_buf.copy_(host_buf)
+    step(**packed)  # warm: the packed views' first call, before capture
+    torch.cuda.synchronize()
+    pgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(pgraph):
+        step(**packed)
+    torch.cuda.synchronize()
+    h2d = total
     acc_h = torch.empty_like(step.accept_len, device="cpu").pin_memory()
     tok_h = torch.empty_like(step.out_tokens, device="cpu").pin_memory()
     d2h = acc_h.numel() * 4 + tok_h.numel() * 4
     stream = torch.cuda.current_stream()
 
     def one(use_graph):
-        for k, v in host.items():
-            if v is not None:
-                dev_set[k].copy_(v, non_blocking=True)
+        dev_buf.copy_(host_buf, non_blocking=True)
         if use_graph:
-            graph.replay()
+            pgraph.replay()
         else:
-            step(**dev_set)
+            step(**packed)
         acc_h.copy_(step.accept_len, non_blocking=True)
         tok_h.copy_(step.out_tokens, non_blocking=True)
         stream.synchronize()
