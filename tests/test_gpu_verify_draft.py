@@ -46,6 +46,10 @@ CASES = {
                         dtype="bf16"),
     "oss-wide": dict(wl="gpt-oss-20b-b64", B=3, V=201088, D=3, k=10, shape=([10], [3, 2, 1], [2, 1]), T=1.0,
                      dtype="bf16"),
+    # vocabularies that split a sequence over 2 CTAs, and over 3 with a shorter last slice
+    "cluster-2": dict(wl="tiny", B=3, V=8192, D=4, k=4, shape=([4], [3, 1], [2, 1], [1]), T=1.0, dtype="bf16"),
+    "cluster-3-ragged": dict(wl="tiny", B=3, V=10000, D=4, k=4, shape=([4], [2, 2], [1, 1], [1]), T=0.8,
+                             dtype="bf16"),
 }
 
 
