@@ -263,9 +263,12 @@ int eagle_tree_mask(const int32_t *node_parent, int B, int n, uint64_t *mask,
  * probabilities rounded to bf16 for the P.V product); fp32 inputs run on the
  * CUDA cores.  Cache rows at or beyond kv_len[b] are never read; every row
  * of k_tree / v_tree must hold finite values.
- * Workspace: none for bf16 (the KV splits of a head merge through the
- * distributed shared memory of one thread-block cluster, so the size is 0);
- * fp32 partial results and weights for fp32.
+ * Workspace (bf16): the KV splits of a head are one thread-block cluster.
+ * When every CTA of a split launch is resident at once (one wave), each CTA
+ * leaves its partial results (fp32 O rows and (m, l) per row) in its own
+ * slot of the workspace and the cluster merges them from L2; other launches
+ * merge through the cluster's distributed shared memory and need none (size
+ * 0).  fp32: partial results and weights.
  * Limits: Hq % Hkv == 0, dh in {64, 128}, 1 <= n <= 4096, B*Hkv <= 65535.
  * ------------------------------------------------------------------------ */
 size_t eagle_tree_attn_workspace_size(int dtype, int B, int n, int Hq, int Hkv,

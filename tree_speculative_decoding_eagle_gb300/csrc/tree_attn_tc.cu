@@ -58,6 +58,12 @@ struct TcArgs {
   float *lse;
   int q_tma;          // 1: Q tiles arrive by TMA (G divides the region's rows), else plain loads
   int32_t *status;
+  // KV split through the workspace (part != nullptr): one slot per CTA,
+  // [slot_rows][DH] fp32 O rows then [slot_rows] (m, l) pairs, the slots of
+  // a cluster consecutive.  Otherwise the split merges through distributed
+  // shared memory.
+  float *part;
+  int slot_rows;
 };
 
 // QR: query rows held per M-tile region.  128 normally; 64 when a group
@@ -97,14 +103,17 @@ struct TcShape {
 // Most KV splits of one (sequence, KV head, M-group): one cluster of CTAs.
 constexpr int kMaxClusterSplits = 8;
 
-// SPLIT: the grid splits the KV range (S > 1) and the kernel carries the
-// cluster merge; without it the merge code is compiled out.
-template <int DH, int MT, int NK, int STAGES, bool SPLIT, int QR>
+// MERGE: 0 the grid does not split the KV range (the merge code is compiled
+// out); 1 the S > 1 splits merge through distributed shared memory; 2 they
+// merge through the workspace.
+template <int DH, int MT, int NK, int STAGES, int MERGE, int QR>
 __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
     tree_attn_tc_kernel(const __grid_constant__ CUtensorMap kc_map, const __grid_constant__ CUtensorMap vc_map,
                         const __grid_constant__ CUtensorMap kt_map, const __grid_constant__ CUtensorMap vt_map,
                         const __grid_constant__ CUtensorMap q_map, TcArgs a) {
   using Sh = TcShape<DH, MT, NK, STAGES, QR>;
+  constexpr bool SPLIT = MERGE != 0;
+  constexpr bool kL2 = MERGE == 2;
   constexpr int NH = NK / 64;  // 64-key halves of a tile
   extern __shared__ unsigned char raw_smem[];
   const uintptr_t raw = reinterpret_cast<uintptr_t>(raw_smem);
@@ -560,39 +569,66 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
         prow[(c0 / 4 + e) ^ (rl & 7)] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
     }
     reinterpret_cast<float2 *>(sQ)[rl] = have ? make_float2(part_m * kLn2, part_l) : make_float2(-INFINITY, 0.f);
-    fence_acq_rel_cluster();
+    if constexpr (!kL2) fence_acq_rel_cluster();
   }
+  const int r0 = mg * MT * 128, nr = max(0, min(rows_total, r0 + MT * 128) - r0);
   if constexpr (SPLIT) {
     tc_fence_before();
     __syncthreads();
+    if constexpr (kL2) {
+      // this CTA's rows [0, nr) into its workspace slot, one 16-byte chunk
+      // per thread and store, a row's chunks contiguous (coalesced)
+      constexpr int NV = DH / 4;
+      const int64_t cl = static_cast<int64_t>(bg) * gridDim.y + mg;
+      float *slot = a.part + (cl * a.S + split) * static_cast<int64_t>(a.slot_rows) * (DH + 2);
+      for (int idx = tid; idx < nr * NV; idx += Sh::kThreads) {
+        const int r = idx / NV, c = idx % NV;
+        reinterpret_cast<float4 *>(slot)[idx] = reinterpret_cast<const float4 *>(sKV)[r * NV + (c ^ (r & 7))];
+      }
+      for (int r = tid; r < nr; r += Sh::kThreads)
+        reinterpret_cast<float2 *>(slot + static_cast<int64_t>(a.slot_rows) * DH)[r] =
+            reinterpret_cast<const float2 *>(sQ)[r];
+    }
   }
   if (warp == mma_warp) tmem_dealloc(tmem, Sh::kTmemCols);
 
   // ---- split merge across the cluster ----------------------------------------
-  // The S splits of this (b, g, M-group) are one cluster.  Each CTA signals
-  // every peer that its partials are in shared memory, then merges rows
-  // [rank*per, (rank+1)*per) of the group by reading all S partials through
-  // distributed shared memory: out = sum_s w_s O_s with w_s = exp(m_s - M) / L,
-  // M = max_s m_s, L = sum_s exp(m_s - M) l_s.  A second round of signals
-  // keeps every CTA's shared memory alive until its peers have read it.
-  // Both waits are bounded; a timeout raises EAGLE_ERR_TIMEOUT.
+  // The S splits of this (b, g, M-group) are one cluster.  Each CTA merges
+  // rows [rank*per, (rank+1)*per) of the group from all S partials:
+  // out = sum_s w_s O_s with w_s = exp(m_s - M) / L, M = max_s m_s,
+  // L = sum_s exp(m_s - M) l_s.  Two forms:
+  //  * workspace (one-wave launches): each CTA has put its unnormalised fp32
+  //    O rows and (m, l) into its slot; after one cluster barrier (release,
+  //    acquire) the rows are read from L2, skipping L1.  Global memory
+  //    outlives every CTA, so no second round is needed.
+  //  * distributed shared memory: each CTA signals every peer that its
+  //    partials are in its shared memory and reads its rows from all of them;
+  //    a second round of signals keeps every CTA's shared memory alive until
+  //    its peers have read it.  Both waits are bounded; a timeout raises
+  //    EAGLE_ERR_TIMEOUT.
   if constexpr (SPLIT) {
     cluster_wait();  // every peer has initialised its barriers
     const uint32_t rank = cluster_ctarank();
-    if (tid < a.S) mbar_arrive_remote(mapa_shared(smem_u32(cl_full), tid));  // one peer per thread
-    // one thread polls; the CTA barrier releases the others
-    if (tid == 0) {
-      *abort_flag = mbar_wait_cluster(cl_full, 0, 200000000ull) ? 0 : 1;
-      if (*abort_flag) report(a.status, EAGLE_ERR_TIMEOUT);
+    if constexpr (kL2) {
+      cluster_arrive_release();
+      cluster_wait();
+    } else {
+      if (tid < a.S) mbar_arrive_remote(mapa_shared(smem_u32(cl_full), tid));  // one peer per thread
+      // one thread polls; the CTA barrier releases the others
+      if (tid == 0) {
+        *abort_flag = mbar_wait_cluster(cl_full, 0, 200000000ull) ? 0 : 1;
+        if (*abort_flag) report(a.status, EAGLE_ERR_TIMEOUT);
+      }
+      __syncthreads();
     }
-    __syncthreads();
     const bool cok = *abort_flag == 0;
-    const int r0 = mg * MT * 128, nr = max(0, min(rows_total, r0 + MT * 128) - r0);
     const int per = (nr + a.S - 1) / a.S;
     const int q0 = min(nr, static_cast<int>(rank) * per), q1 = min(nr, q0 + per);
     uint32_t r_o[kMaxClusterSplits];  // the peers' O buffers
 #pragma unroll
     for (int sp = 0; sp < kMaxClusterSplits; ++sp) r_o[sp] = mapa_shared(smem_u32(sKV), sp < a.S ? sp : 0);
+    const int64_t slot_floats = static_cast<int64_t>(a.slot_rows) * (DH + 2);
+    const float *slots = kL2 ? a.part + (static_cast<int64_t>(bg) * gridDim.y + mg) * a.S * slot_floats : nullptr;
     // four output columns per item, two items per thread at a time.  The NV
     // items of a row sit in NV consecutive lanes: lane c of the row loads
     // split c's (m, l) and the row's lanes share them by shuffles; every
@@ -610,11 +646,21 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
         const int item = base + u * Sh::kThreads;
         const int rr = q0 + item / NV, c = item % NV;
         const bool valid = item < n_items;
-        mine[u] = (valid && c < a.S) ? ld_cluster_f2(mapa_shared(ml_local, c) + rr * 8) : make_float2(-INFINITY, 0.f);
-        const uint32_t off = static_cast<uint32_t>((rr * NV + (c ^ (rr & 7))) * 16);
+        if constexpr (kL2) {
+          mine[u] = (valid && c < a.S)
+                        ? __ldcg(reinterpret_cast<const float2 *>(slots + c * slot_floats + static_cast<int64_t>(a.slot_rows) * DH) + rr)
+                        : make_float2(-INFINITY, 0.f);
 #pragma unroll
-        for (int sp = 0; sp < kMaxClusterSplits; ++sp)
-          po[u][sp] = (valid && sp < a.S) ? ld_cluster_f4(r_o[sp] + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int sp = 0; sp < kMaxClusterSplits; ++sp)
+            po[u][sp] = (valid && sp < a.S) ? __ldcg(reinterpret_cast<const float4 *>(slots + sp * slot_floats) + rr * NV + c)
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+          mine[u] = (valid && c < a.S) ? ld_cluster_f2(mapa_shared(ml_local, c) + rr * 8) : make_float2(-INFINITY, 0.f);
+          const uint32_t off = static_cast<uint32_t>((rr * NV + (c ^ (rr & 7))) * 16);
+#pragma unroll
+          for (int sp = 0; sp < kMaxClusterSplits; ++sp)
+            po[u][sp] = (valid && sp < a.S) ? ld_cluster_f4(r_o[sp] + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
 #pragma unroll
       for (int u = 0; u < kItems; ++u) {
@@ -653,10 +699,12 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
         if (c == 0 && a.lse) a.lse[orow] = Ls > 0.f ? M + __logf(Ls) : -INFINITY;
       }
     }
-    __syncthreads();  // this CTA is done reading its peers
-    if (tid < a.S) mbar_arrive_remote(mapa_shared(smem_u32(cl_done), tid));
-    // stay (and keep this CTA's shared memory) until every peer is done
-    if (tid == 0 && !mbar_wait_cluster(cl_done, 0, 200000000ull)) report(a.status, EAGLE_ERR_TIMEOUT);
+    if constexpr (!kL2) {
+      __syncthreads();  // this CTA is done reading its peers
+      if (tid < a.S) mbar_arrive_remote(mapa_shared(smem_u32(cl_done), tid));
+      // stay (and keep this CTA's shared memory) until every peer is done
+      if (tid == 0 && !mbar_wait_cluster(cl_done, 0, 200000000ull)) report(a.status, EAGLE_ERR_TIMEOUT);
+    }
   }
 }
 
@@ -742,28 +790,48 @@ static TcPlan tc_plan(int B, int n, int Hq, int Hkv, int dh, int Lmax, int num_s
   return p;
 }
 
-// The splits merge through distributed shared memory: no workspace.
-size_t attn_tc_workspace_bytes(int, int, int, int, int, int, int) { return 0; }
+// Rows of a split's workspace slot: the most (node, grouped head) rows of an
+// M-group, rounded up to 8.
+static int tc_slot_rows(const TcPlan &p, int n, int G) {
+  const int rows = (n * G + 7) / 8 * 8;
+  return rows < p.MT * 128 ? rows : p.MT * 128;
+}
 
-template <int DH, int MT, int NK, int STAGES, bool SPLIT, int QR>
+// A split launch whose CTAs are all resident at once (one wave) passes its
+// partial results through the workspace, one slot of fp32 O rows and (m, l)
+// pairs per CTA, read back from L2; launches of more waves, where the extra
+// write traffic costs more than it saves, merge through distributed shared
+// memory and need none.
+static bool tc_merge_in_workspace(const TcPlan &p, int B, int Hkv, int num_sms) {
+  return p.S > 1 && static_cast<int64_t>(B) * Hkv * p.mgroups * p.S <= static_cast<int64_t>(num_sms) * p.ctas_per_sm;
+}
+
+size_t attn_tc_workspace_bytes(int B, int n, int Hq, int Hkv, int dh, int Lmax, int num_sms) {
+  const TcPlan p = tc_plan(B, n, Hq, Hkv, dh, Lmax, num_sms);
+  if (!tc_merge_in_workspace(p, B, Hkv, num_sms)) return 0;
+  return static_cast<size_t>(B) * Hkv * p.mgroups * p.S * tc_slot_rows(p, n, Hq / Hkv) * (dh + 2) * sizeof(float);
+}
+
+template <int DH, int MT, int NK, int STAGES, int MERGE, int QR>
 static cudaError_t launch_tc_v(const CUtensorMap *maps, const TcArgs &a, const TcPlan &p, cudaStream_t st) {
   using Sh = TcShape<DH, MT, NK, STAGES, QR>;
   static_assert(Sh::kSmem <= 232448, "shared memory budget");
   // MT = 1 variants run two CTAs per SM (228 KB per SM, 1 KB reserved per CTA)
   static_assert(MT != 1 || 2 * (Sh::kSmem + 1024) <= 233472, "two CTAs per SM");
   static std::atomic<unsigned long long> configured{0};
-  const cudaError_t e = set_smem_limit_once(tree_attn_tc_kernel<DH, MT, NK, STAGES, SPLIT, QR>, Sh::kSmem, configured);
+  const cudaError_t e = set_smem_limit_once(tree_attn_tc_kernel<DH, MT, NK, STAGES, MERGE, QR>, Sh::kSmem, configured);
   if (e != cudaSuccess) return e;
   // the S splits of one (b, g, M-group) form one cluster
   dim3 grid(p.S, p.mgroups, a.B * a.Hkv);
-  return launch_chained_cluster(tree_attn_tc_kernel<DH, MT, NK, STAGES, SPLIT, QR>, grid, dim3(Sh::kThreads), Sh::kSmem,
+  return launch_chained_cluster(tree_attn_tc_kernel<DH, MT, NK, STAGES, MERGE, QR>, grid, dim3(Sh::kThreads), Sh::kSmem,
                                 st, p.S, maps[0], maps[1], maps[2], maps[3], maps[4], a);
 }
 
 template <int DH, int MT, int NK, int STAGES, int QR = 128>
 static cudaError_t launch_tc_t(const CUtensorMap *maps, const TcArgs &a, const TcPlan &p, cudaStream_t st) {
-  return p.S > 1 ? launch_tc_v<DH, MT, NK, STAGES, true, QR>(maps, a, p, st)
-                 : launch_tc_v<DH, MT, NK, STAGES, false, QR>(maps, a, p, st);
+  if (p.S <= 1) return launch_tc_v<DH, MT, NK, STAGES, 0, QR>(maps, a, p, st);
+  return a.part ? launch_tc_v<DH, MT, NK, STAGES, 2, QR>(maps, a, p, st)
+                : launch_tc_v<DH, MT, NK, STAGES, 1, QR>(maps, a, p, st);
 }
 
 // Common launcher; block_table == nullptr is the contiguous cache, otherwise
@@ -805,6 +873,9 @@ static cudaError_t launch_tc_common(const void *q, const void *k_cache, const vo
   a.lse = lse;
   a.q_tma = q_tma ? 1 : 0;
   a.status = status;
+  a.part = tc_merge_in_workspace(p, B, Hkv, num_sms) ? reinterpret_cast<float *>(ws) : nullptr;
+  a.slot_rows = tc_slot_rows(p, n, G);
+  if (tc_merge_in_workspace(p, B, Hkv, num_sms) && !ws) return cudaErrorInvalidValue;
   cudaError_t e;
   // stages: as many as shared memory allows at the variant's CTAs per SM
   if (dh == 64) {
