@@ -2,7 +2,9 @@
 
 When few (sequence, KV head, M-group) work items exist, the launch splits the
 KV range S ways and the S CTAs of an item form a thread-block cluster that
-merges its partial results through distributed shared memory.  These shapes
+merges its partial results: through the workspace when the launch is one wave
+(every case here), else through distributed shared memory (the 13B-shaped
+parity case).  These shapes
 make the launch plan pick S = 1..8, with one and two 128-row M-tiles per CTA
 and both head sizes; lengths are ragged (one sequence may have an empty
 prefix, leaving whole splits empty) and every case runs twice on the same
