@@ -85,14 +85,13 @@ def algorithmic(w, kv_len, depth_sum):
 
 def launches_per_step(w):
     """Kernels one step launches: draft top-k 1, tree build (mask fused) 1,
-    tree attention 1 (fp32: +1 combine when the KV prefix is split, i.e.
-    when it asks for a workspace), verification 2 (chunk statistics, walk)."""
+    tree attention 1 or 2 (as the library reports: a split launch of several
+    waves, or a split fp32 launch, adds a merge kernel), verification 2
+    (chunk statistics, walk)."""
     import tree_speculative_decoding_eagle_gb300 as eg
     dt = eg.BF16 if w.dtype == "bf16" else eg.F32
-    # bf16 attention merges KV splits inside its own kernel; the fp32 path
-    # launches a combine kernel when it splits
-    split = eg.load_library().eagle_tree_attn_workspace_size(dt, w.B, w.n_nodes, w.Hq, w.Hkv, w.dh, w.L) > 0
-    return {"draft_topk": 1, "tree_build": 1, "tree_attn": 2 if (split and w.dtype != "bf16") else 1, "verify": 2}
+    attn = eg.load_library().eagle_tree_attn_kernel_count(dt, w.B, w.n_nodes, w.Hq, w.Hkv, w.dh, w.L)
+    return {"draft_topk": 1, "tree_build": 1, "tree_attn": attn, "verify": 2}
 
 
 def load_peaks():

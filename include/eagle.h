@@ -263,16 +263,23 @@ int eagle_tree_mask(const int32_t *node_parent, int B, int n, uint64_t *mask,
  * probabilities rounded to bf16 for the P.V product); fp32 inputs run on the
  * CUDA cores.  Cache rows at or beyond kv_len[b] are never read; every row
  * of k_tree / v_tree must hold finite values.
- * Workspace (bf16): the KV splits of a head are one thread-block cluster.
- * When every CTA of a split launch is resident at once (one wave), each CTA
- * leaves its partial results (fp32 O rows and (m, l) per row) in its own
- * slot of the workspace and the cluster merges them from L2; other launches
- * merge through the cluster's distributed shared memory and need none (size
- * 0).  fp32: partial results and weights.
+ * Workspace (bf16): a launch that splits the KV prefix of a head over
+ * several CTAs needs one slot per CTA (fp32 O rows and (m, l) per row); each
+ * CTA leaves its partial results there.  When every CTA of the launch is
+ * resident at once (one wave) the splits of a head are one thread-block
+ * cluster and merge from L2 after a cluster barrier; otherwise a second
+ * kernel merges them.  An unsplit launch needs none (size 0).  fp32:
+ * partial results and weights.
  * Limits: Hq % Hkv == 0, dh in {64, 128}, 1 <= n <= 4096, B*Hkv <= 65535.
  * ------------------------------------------------------------------------ */
 size_t eagle_tree_attn_workspace_size(int dtype, int B, int n, int Hq, int Hkv,
                                       int dh, int Lmax);
+
+/* Kernels one eagle_tree_attn call with these arguments launches (1 or 2:
+ * the attention, and the merge of a split launch of several waves, or the
+ * fp32 combine); 0 for invalid arguments.  Host only. */
+int eagle_tree_attn_kernel_count(int dtype, int B, int n, int Hq, int Hkv,
+                                 int dh, int Lmax);
 
 int eagle_tree_attn(const void *q, const void *k_cache, const void *v_cache,
                     const int32_t *kv_len, const void *k_tree,

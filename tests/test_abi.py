@@ -101,3 +101,12 @@ def test_workspace_queries_are_host_only(lib):
     assert lib.eagle_draft_topk_workspace_size(1, 6, 10, 32000) == 0   # parts merge in cluster shared memory
     assert lib.eagle_draft_topk_workspace_size(64, 6, 10, 201088) == 0
     assert lib.eagle_draft_topk_workspace_size(0, 6, 10, 32000) == 0
+    # attention: one kernel unless a split launch needs a merge kernel; a
+    # split launch asks for a workspace slot per CTA
+    BF16 = eg.BF16
+    assert lib.eagle_tree_attn_kernel_count(BF16, 1, 61, 32, 32, 128, 2048) == 1   # one wave, cluster merge
+    assert lib.eagle_tree_attn_workspace_size(BF16, 1, 61, 32, 32, 128, 2048) > 0
+    assert lib.eagle_tree_attn_kernel_count(BF16, 64, 61, 64, 8, 64, 8192) == 1    # unsplit
+    assert lib.eagle_tree_attn_workspace_size(BF16, 64, 61, 64, 8, 64, 8192) == 0
+    assert lib.eagle_tree_attn_kernel_count(BF16, 8, 51, 40, 40, 128, 4096) == 2   # several waves: merge kernel
+    assert lib.eagle_tree_attn_kernel_count(BF16, 0, 61, 32, 32, 128, 2048) == 0

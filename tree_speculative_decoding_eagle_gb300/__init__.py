@@ -35,7 +35,7 @@ EXPORTED = (
     "eagle_status_string", "eagle_version", "eagle_selftest_wait",
     "eagle_draft_topk_workspace_size", "eagle_draft_topk",
     "eagle_tree_build", "eagle_tree_build_variant", "eagle_static_tree", "eagle_tree_mask",
-    "eagle_tree_attn_workspace_size", "eagle_tree_attn",
+    "eagle_tree_attn_workspace_size", "eagle_tree_attn_kernel_count", "eagle_tree_attn",
     "eagle_tree_attn_paged_workspace_size", "eagle_tree_attn_paged", "eagle_kv_commit",
     "eagle_verify_workspace_size", "eagle_verify", "eagle_verify_noalloc", "eagle_verify_draft",
 )
@@ -67,6 +67,7 @@ def load_library(path=LIB_PATH):
         "eagle_static_tree": (I, [P, P, I, I, I, P, P, I, P, P, P, P, P, P, P, P, P, P]),
         "eagle_tree_mask": (I, [P, I, I, P, P]),
         "eagle_tree_attn_workspace_size": (SZ, [I, I, I, I, I, I, I]),
+        "eagle_tree_attn_kernel_count": (I, [I, I, I, I, I, I, I]),
         "eagle_tree_attn": (I, [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, P, P, P, SZ, P]),
         "eagle_tree_attn_paged_workspace_size": (SZ, [I, I, I, I, I, I, I, I]),
         "eagle_tree_attn_paged": (I, [P, P, P, P, I, I, I, P, P, P, P, I, I, I, I, I, I, F, P, P, P, P, SZ, P]),

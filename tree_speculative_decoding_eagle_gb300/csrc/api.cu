@@ -50,6 +50,7 @@ cudaError_t launch_tree_attn_simt(const void *q, const void *k_cache, const void
                                   int dh, int Lmax, float scale, void *out, float *lse, void *ws,
                                   int num_sms, cudaStream_t st);
 size_t attn_tc_workspace_bytes(int B, int n, int Hq, int Hkv, int dh, int Lmax, int num_sms);
+int attn_tc_kernel_count(int B, int n, int Hq, int Hkv, int dh, int Lmax, int num_sms);
 cudaError_t launch_tree_attn_tc(const void *q, const void *k_cache, const void *v_cache, const int32_t *kv_len,
                                 const void *k_tree, const void *v_tree, const uint64_t *mask, int B, int n,
                                 int Hq, int Hkv, int dh, int Lmax, float scale, void *out, float *lse, void *ws,
@@ -168,6 +169,13 @@ size_t eagle_tree_attn_workspace_size(int dtype, int B, int n, int Hq, int Hkv, 
   if (B < 1 || n < 1 || Hq < 1 || Hkv < 1 || dh < 1 || Lmax < 0) return 0;
   if (dtype == EAGLE_BF16) return attn_tc_workspace_bytes(B, n, Hq, Hkv, dh, Lmax, current_num_sms());
   return attn_simt_workspace_bytes(B, n, Hq, dh, Lmax, current_num_sms());
+}
+
+int eagle_tree_attn_kernel_count(int dtype, int B, int n, int Hq, int Hkv, int dh, int Lmax) {
+  if (!valid_dtype(dtype) || B < 1 || n < 1 || Hq < 1 || Hkv < 1 || dh < 1 || Lmax < 0) return 0;
+  if (dtype == EAGLE_BF16) return attn_tc_kernel_count(B, n, Hq, Hkv, dh, Lmax, current_num_sms());
+  // fp32: a split prefix adds the combine kernel (it asks for a workspace)
+  return attn_simt_workspace_bytes(B, n, Hq, dh, Lmax, current_num_sms()) > 0 ? 2 : 1;
 }
 
 int eagle_tree_attn(const void *q, const void *k_cache, const void *v_cache, const int32_t *kv_len,

@@ -27,10 +27,12 @@
 //     only when the running maximum grows by more than 2^8.  A warp whose 32
 //     rows all lie past the last (node, head) row only signals.
 // Tensor memory per M-tile: S (NK columns), P (NK/2), O (dh).
-// KV split (few heads: S <= 8 CTAs share one (b, g, M-group)): the S CTAs
-// are one thread-block cluster; each leaves its unnormalised O and (m, l)
-// in its own shared memory and merges 1/S of the rows from all S through
-// distributed shared memory, so partial results never reach HBM.
+// KV split (few heads: S <= 8 CTAs share one (b, g, M-group)): each CTA
+// leaves its unnormalised fp32 O rows and (m, l) in its own workspace slot.
+// When the launch is one wave the S CTAs are one thread-block cluster and
+// each merges 1/S of the rows from all S slots after a cluster barrier;
+// otherwise the CTAs leave at once (no co-scheduling, no waiting on peers)
+// and tree_attn_merge_kernel merges.  The slots are read back from L2.
 // Every wait is bounded; a timeout raises EAGLE_ERR_TIMEOUT in the status
 // word and the CTA drains its copies and MMAs, frees tensor memory and exits.
 #include <mutex>
@@ -79,7 +81,7 @@ struct TcShape {
   static constexpr int kTileBytes = kRegions * NK * 128;     // one K (or V) tile
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kBarOff = kQBytes + STAGES * kStageBytes;
-  static constexpr int kNumBars = 2 * STAGES + 4 * MT + 4;
+  static constexpr int kNumBars = 2 * STAGES + 4 * MT + 2;
   static constexpr int kBarBytes = kNumBars * 8 + 16;
   // QR = 128: buffers at the first 1 KB boundary, barriers after them.
   // QR = 64: the barriers sit in the gap before the 1 KB-aligned buffers
@@ -104,8 +106,9 @@ struct TcShape {
 constexpr int kMaxClusterSplits = 8;
 
 // MERGE: 0 the grid does not split the KV range (the merge code is compiled
-// out); 1 the S > 1 splits merge through distributed shared memory; 2 they
-// merge through the workspace.
+// out); otherwise every CTA leaves its partial results in its workspace slot
+// and 1 the S splits of an item (one cluster) merge after a cluster barrier,
+// 2 tree_attn_merge_kernel merges them.
 template <int DH, int MT, int NK, int STAGES, int MERGE, int QR>
 __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
     tree_attn_tc_kernel(const __grid_constant__ CUtensorMap kc_map, const __grid_constant__ CUtensorMap vc_map,
@@ -113,7 +116,7 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
                         const __grid_constant__ CUtensorMap q_map, TcArgs a) {
   using Sh = TcShape<DH, MT, NK, STAGES, QR>;
   constexpr bool SPLIT = MERGE != 0;
-  constexpr bool kL2 = MERGE == 2;
+  constexpr bool kCluster = MERGE == 1;  // the splits merge in this kernel
   constexpr int NH = NK / 64;  // 64-key halves of a tile
   extern __shared__ unsigned char raw_smem[];
   const uintptr_t raw = reinterpret_cast<uintptr_t>(raw_smem);
@@ -136,8 +139,6 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
   uint64_t *o_done = p_full + MT;
   uint64_t *teardown = o_done + MT;
   uint64_t *q_full = teardown + 1;  // the Q tiles (TMA)
-  uint64_t *cl_full = q_full + 1; // split merge: every CTA of the cluster has its partials in shared memory
-  uint64_t *cl_done = cl_full + 1;  // split merge: every CTA of the cluster has read its peers
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Sh::kNumBars);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -189,10 +190,6 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
     }
     mbar_init(teardown, 1);
     mbar_init(q_full, 1);
-    if constexpr (SPLIT) {
-      mbar_init(cl_full, a.S);
-      mbar_init(cl_done, a.S);
-    }
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -203,7 +200,6 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if constexpr (SPLIT) cluster_arrive_relaxed();  // waited on before the first signal to a peer
   const uint32_t tmem = *tmem_slot;
 
   int issued = 0;  // producer: tiles issued
@@ -569,13 +565,12 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
         prow[(c0 / 4 + e) ^ (rl & 7)] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
     }
     reinterpret_cast<float2 *>(sQ)[rl] = have ? make_float2(part_m * kLn2, part_l) : make_float2(-INFINITY, 0.f);
-    if constexpr (!kL2) fence_acq_rel_cluster();
   }
   const int r0 = mg * MT * 128, nr = max(0, min(rows_total, r0 + MT * 128) - r0);
   if constexpr (SPLIT) {
     tc_fence_before();
     __syncthreads();
-    if constexpr (kL2) {
+    {
       // this CTA's rows [0, nr) into its workspace slot, one 16-byte chunk
       // per thread and store, a row's chunks contiguous (coalesced)
       constexpr int NV = DH / 4;
@@ -593,42 +588,22 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
   if (warp == mma_warp) tmem_dealloc(tmem, Sh::kTmemCols);
 
   // ---- split merge across the cluster ----------------------------------------
-  // The S splits of this (b, g, M-group) are one cluster.  Each CTA merges
-  // rows [rank*per, (rank+1)*per) of the group from all S partials:
-  // out = sum_s w_s O_s with w_s = exp(m_s - M) / L, M = max_s m_s,
-  // L = sum_s exp(m_s - M) l_s.  Two forms:
-  //  * workspace (one-wave launches): each CTA has put its unnormalised fp32
-  //    O rows and (m, l) into its slot; after one cluster barrier (release,
-  //    acquire) the rows are read from L2, skipping L1.  Global memory
-  //    outlives every CTA, so no second round is needed.
-  //  * distributed shared memory: each CTA signals every peer that its
-  //    partials are in its shared memory and reads its rows from all of them;
-  //    a second round of signals keeps every CTA's shared memory alive until
-  //    its peers have read it.  Both waits are bounded; a timeout raises
-  //    EAGLE_ERR_TIMEOUT.
-  if constexpr (SPLIT) {
-    cluster_wait();  // every peer has initialised its barriers
+  // One-wave split launches (MERGE = 1): the S splits of this (b, g,
+  // M-group) are one cluster.  Each CTA has put its unnormalised fp32 O rows
+  // and (m, l) into its workspace slot; after one cluster barrier (release,
+  // acquire) it merges rows [rank*per, (rank+1)*per) of the group from all S
+  // slots, read from L2 skipping L1: out = sum_s w_s O_s with
+  // w_s = exp(m_s - M) / L, M = max_s m_s, L = sum_s exp(m_s - M) l_s.
+  // Global memory outlives every CTA, so no second round is needed.
+  if constexpr (kCluster) {
+    cluster_arrive_release();
+    cluster_wait();
     const uint32_t rank = cluster_ctarank();
-    if constexpr (kL2) {
-      cluster_arrive_release();
-      cluster_wait();
-    } else {
-      if (tid < a.S) mbar_arrive_remote(mapa_shared(smem_u32(cl_full), tid));  // one peer per thread
-      // one thread polls; the CTA barrier releases the others
-      if (tid == 0) {
-        *abort_flag = mbar_wait_cluster(cl_full, 0, 200000000ull) ? 0 : 1;
-        if (*abort_flag) report(a.status, EAGLE_ERR_TIMEOUT);
-      }
-      __syncthreads();
-    }
     const bool cok = *abort_flag == 0;
     const int per = (nr + a.S - 1) / a.S;
     const int q0 = min(nr, static_cast<int>(rank) * per), q1 = min(nr, q0 + per);
-    uint32_t r_o[kMaxClusterSplits];  // the peers' O buffers
-#pragma unroll
-    for (int sp = 0; sp < kMaxClusterSplits; ++sp) r_o[sp] = mapa_shared(smem_u32(sKV), sp < a.S ? sp : 0);
     const int64_t slot_floats = static_cast<int64_t>(a.slot_rows) * (DH + 2);
-    const float *slots = kL2 ? a.part + (static_cast<int64_t>(bg) * gridDim.y + mg) * a.S * slot_floats : nullptr;
+    const float *slots = a.part + (static_cast<int64_t>(bg) * gridDim.y + mg) * a.S * slot_floats;
     // four output columns per item, two items per thread at a time.  The NV
     // items of a row sit in NV consecutive lanes: lane c of the row loads
     // split c's (m, l) and the row's lanes share them by shuffles; every
@@ -637,7 +612,6 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
     static_assert(NV == 16 || NV == 32, "a row's items fill half or all of a warp");
     constexpr int kItems = 2;
     const int n_items = (q1 - q0) * NV;  // a multiple of NV: a row's lanes agree on validity
-    const uint32_t ml_local = smem_u32(sQ);
     for (int base = tid; cok && base - lane < n_items; base += kItems * Sh::kThreads) {
       float2 mine[kItems];
       float4 po[kItems][kMaxClusterSplits];
@@ -646,21 +620,13 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
         const int item = base + u * Sh::kThreads;
         const int rr = q0 + item / NV, c = item % NV;
         const bool valid = item < n_items;
-        if constexpr (kL2) {
-          mine[u] = (valid && c < a.S)
-                        ? __ldcg(reinterpret_cast<const float2 *>(slots + c * slot_floats + static_cast<int64_t>(a.slot_rows) * DH) + rr)
-                        : make_float2(-INFINITY, 0.f);
+        mine[u] = (valid && c < a.S)
+                      ? __ldcg(reinterpret_cast<const float2 *>(slots + c * slot_floats + static_cast<int64_t>(a.slot_rows) * DH) + rr)
+                      : make_float2(-INFINITY, 0.f);
 #pragma unroll
-          for (int sp = 0; sp < kMaxClusterSplits; ++sp)
-            po[u][sp] = (valid && sp < a.S) ? __ldcg(reinterpret_cast<const float4 *>(slots + sp * slot_floats) + rr * NV + c)
-                                            : make_float4(0.f, 0.f, 0.f, 0.f);
-        } else {
-          mine[u] = (valid && c < a.S) ? ld_cluster_f2(mapa_shared(ml_local, c) + rr * 8) : make_float2(-INFINITY, 0.f);
-          const uint32_t off = static_cast<uint32_t>((rr * NV + (c ^ (rr & 7))) * 16);
-#pragma unroll
-          for (int sp = 0; sp < kMaxClusterSplits; ++sp)
-            po[u][sp] = (valid && sp < a.S) ? ld_cluster_f4(r_o[sp] + off) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+        for (int sp = 0; sp < kMaxClusterSplits; ++sp)
+          po[u][sp] = (valid && sp < a.S) ? __ldcg(reinterpret_cast<const float4 *>(slots + sp * slot_floats) + rr * NV + c)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int u = 0; u < kItems; ++u) {
@@ -699,13 +665,47 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
         if (c == 0 && a.lse) a.lse[orow] = Ls > 0.f ? M + __logf(Ls) : -INFINITY;
       }
     }
-    if constexpr (!kL2) {
-      __syncthreads();  // this CTA is done reading its peers
-      if (tid < a.S) mbar_arrive_remote(mapa_shared(smem_u32(cl_done), tid));
-      // stay (and keep this CTA's shared memory) until every peer is done
-      if (tid == 0 && !mbar_wait_cluster(cl_done, 0, 200000000ull)) report(a.status, EAGLE_ERR_TIMEOUT);
-    }
   }
+}
+
+// The merge of a split launch of several waves (MERGE = 2): one thread per (row, 4 output columns) of a
+// (b, g, M-group), out = sum_s w_s O_s with w_s = exp(m_s - M) / L,
+// M = max_s m_s, L = sum_s exp(m_s - M) l_s, reading the S slots from L2.
+template <int DH>
+__global__ void __launch_bounds__(256) tree_attn_merge_kernel(TcArgs a, int MT) {
+  constexpr int NV = DH / 4;
+  const int mg = blockIdx.y, bg = blockIdx.z, b = bg / a.Hkv, g = bg % a.Hkv;
+  const int rows_total = a.n * a.G;
+  const int r0 = mg * MT * 128, nr = max(0, min(rows_total, r0 + MT * 128) - r0);
+  const int item = blockIdx.x * blockDim.x + threadIdx.x;
+  pdl_wait();  // the partial results come from the attention kernel
+  if (item >= nr * NV) return;
+  const int rr = item / NV, c = item % NV;
+  const int64_t slot_floats = static_cast<int64_t>(a.slot_rows) * (DH + 2);
+  const float *slots = a.part + (static_cast<int64_t>(bg) * gridDim.y + mg) * a.S * slot_floats;
+  float M = -INFINITY;
+  for (int sp = 0; sp < a.S; ++sp)
+    M = fmaxf(M, __ldcg(reinterpret_cast<const float2 *>(slots + sp * slot_floats + static_cast<int64_t>(a.slot_rows) * DH) + rr).x);
+  float Ls = 0.f;
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int sp = 0; sp < a.S; ++sp) {
+    const float2 ml = __ldcg(reinterpret_cast<const float2 *>(slots + sp * slot_floats + static_cast<int64_t>(a.slot_rows) * DH) + rr);
+    const float4 po = __ldcg(reinterpret_cast<const float4 *>(slots + sp * slot_floats) + rr * NV + c);
+    const float wgt = (M > -INFINITY && ml.x > -INFINITY) ? ex2_approx((ml.x - M) * kLog2e) : 0.f;
+    Ls = fmaf(wgt, ml.y, Ls);
+    o.x = fmaf(wgt, po.x, o.x); o.y = fmaf(wgt, po.y, o.y);
+    o.z = fmaf(wgt, po.z, o.z); o.w = fmaf(wgt, po.w, o.w);
+  }
+  const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+  const int rho = r0 + rr, i = rho / a.G, h = g * a.G + rho % a.G;
+  const int64_t orow = (static_cast<int64_t>(b) * a.n + i) * a.Hq + h;
+  __nv_bfloat162 lo = __floats2bfloat162_rn(o.x * inv, o.y * inv);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(o.z * inv, o.w * inv);
+  uint2 packed;
+  packed.x = *reinterpret_cast<const uint32_t *>(&lo);
+  packed.y = *reinterpret_cast<const uint32_t *>(&hi);
+  reinterpret_cast<uint2 *>(a.out + orow * DH)[c] = packed;
+  if (c == 0 && a.lse) a.lse[orow] = Ls > 0.f ? M + __logf(Ls) : -INFINITY;
 }
 
 // ---- host side ---------------------------------------------------------------
@@ -757,7 +757,7 @@ static bool make_q_map(CUtensorMap *map, const void *base, int64_t rows, int Hq,
 }
 
 struct TcPlan {
-  int MT, NK, mgroups, S, ctas_per_sm;
+  int MT, NK, mgroups, S, ctas_per_sm, num_sms;
 };
 
 // Launch plan: M-tiles per CTA, key-tile width, and the KV split S chosen to
@@ -765,6 +765,7 @@ struct TcPlan {
 // split's partial results, in key-tile units).
 static TcPlan tc_plan(int B, int n, int Hq, int Hkv, int dh, int Lmax, int num_sms) {
   TcPlan p;
+  p.num_sms = num_sms;
   const int G = Hq / Hkv;
   const int tiles = (n * G + 127) / 128;
   p.MT = tiles <= 1 ? 1 : 2;
@@ -797,18 +798,26 @@ static int tc_slot_rows(const TcPlan &p, int n, int G) {
   return rows < p.MT * 128 ? rows : p.MT * 128;
 }
 
-// A split launch whose CTAs are all resident at once (one wave) passes its
-// partial results through the workspace, one slot of fp32 O rows and (m, l)
-// pairs per CTA, read back from L2; launches of more waves, where the extra
-// write traffic costs more than it saves, merge through distributed shared
-// memory and need none.
-static bool tc_merge_in_workspace(const TcPlan &p, int B, int Hkv, int num_sms) {
-  return p.S > 1 && static_cast<int64_t>(B) * Hkv * p.mgroups * p.S <= static_cast<int64_t>(num_sms) * p.ctas_per_sm;
+// A split launch passes its partial results through the workspace, one slot
+// of fp32 O rows and (m, l) pairs per CTA, read back from L2.  When its CTAs
+// are all resident at once (one wave) the splits of an item are one cluster
+// and merge after a cluster barrier; otherwise every CTA leaves as soon as
+// its slot is written (no cluster co-scheduling, no waiting on peers) and a
+// second kernel merges.
+static bool tc_one_wave(const TcPlan &p, int B, int Hkv, int num_sms) {
+  return static_cast<int64_t>(B) * Hkv * p.mgroups * p.S <= static_cast<int64_t>(num_sms) * p.ctas_per_sm;
+}
+
+// Kernels one launch runs: the attention, plus the merge for a split
+// launch of several waves.
+int attn_tc_kernel_count(int B, int n, int Hq, int Hkv, int dh, int Lmax, int num_sms) {
+  const TcPlan p = tc_plan(B, n, Hq, Hkv, dh, Lmax, num_sms);
+  return p.S > 1 && !tc_one_wave(p, B, Hkv, num_sms) ? 2 : 1;
 }
 
 size_t attn_tc_workspace_bytes(int B, int n, int Hq, int Hkv, int dh, int Lmax, int num_sms) {
   const TcPlan p = tc_plan(B, n, Hq, Hkv, dh, Lmax, num_sms);
-  if (!tc_merge_in_workspace(p, B, Hkv, num_sms)) return 0;
+  if (p.S <= 1) return 0;
   return static_cast<size_t>(B) * Hkv * p.mgroups * p.S * tc_slot_rows(p, n, Hq / Hkv) * (dh + 2) * sizeof(float);
 }
 
@@ -821,8 +830,16 @@ static cudaError_t launch_tc_v(const CUtensorMap *maps, const TcArgs &a, const T
   static std::atomic<unsigned long long> configured{0};
   const cudaError_t e = set_smem_limit_once(tree_attn_tc_kernel<DH, MT, NK, STAGES, MERGE, QR>, Sh::kSmem, configured);
   if (e != cudaSuccess) return e;
-  // the S splits of one (b, g, M-group) form one cluster
   dim3 grid(p.S, p.mgroups, a.B * a.Hkv);
+  if constexpr (MERGE == 2) {
+    cudaError_t le = launch_chained(tree_attn_tc_kernel<DH, MT, NK, STAGES, MERGE, QR>, grid, dim3(Sh::kThreads),
+                                    Sh::kSmem, st, maps[0], maps[1], maps[2], maps[3], maps[4], a);
+    if (le != cudaSuccess) return le;
+    const int rows = a.slot_rows;  // at least any M-group's rows
+    const dim3 mgrid((rows * (DH / 4) + 255) / 256, p.mgroups, a.B * a.Hkv);
+    return launch_chained(tree_attn_merge_kernel<DH>, mgrid, dim3(256), 0, st, a, MT);
+  }
+  // the S splits of one (b, g, M-group) form one cluster
   return launch_chained_cluster(tree_attn_tc_kernel<DH, MT, NK, STAGES, MERGE, QR>, grid, dim3(Sh::kThreads), Sh::kSmem,
                                 st, p.S, maps[0], maps[1], maps[2], maps[3], maps[4], a);
 }
@@ -830,8 +847,8 @@ static cudaError_t launch_tc_v(const CUtensorMap *maps, const TcArgs &a, const T
 template <int DH, int MT, int NK, int STAGES, int QR = 128>
 static cudaError_t launch_tc_t(const CUtensorMap *maps, const TcArgs &a, const TcPlan &p, cudaStream_t st) {
   if (p.S <= 1) return launch_tc_v<DH, MT, NK, STAGES, 0, QR>(maps, a, p, st);
-  return a.part ? launch_tc_v<DH, MT, NK, STAGES, 2, QR>(maps, a, p, st)
-                : launch_tc_v<DH, MT, NK, STAGES, 1, QR>(maps, a, p, st);
+  return tc_one_wave(p, a.B, a.Hkv, p.num_sms) ? launch_tc_v<DH, MT, NK, STAGES, 1, QR>(maps, a, p, st)
+                                              : launch_tc_v<DH, MT, NK, STAGES, 2, QR>(maps, a, p, st);
 }
 
 // Common launcher; block_table == nullptr is the contiguous cache, otherwise
@@ -873,9 +890,9 @@ static cudaError_t launch_tc_common(const void *q, const void *k_cache, const vo
   a.lse = lse;
   a.q_tma = q_tma ? 1 : 0;
   a.status = status;
-  a.part = tc_merge_in_workspace(p, B, Hkv, num_sms) ? reinterpret_cast<float *>(ws) : nullptr;
+  a.part = p.S > 1 ? reinterpret_cast<float *>(ws) : nullptr;
   a.slot_rows = tc_slot_rows(p, n, G);
-  if (tc_merge_in_workspace(p, B, Hkv, num_sms) && !ws) return cudaErrorInvalidValue;
+  if (p.S > 1 && !ws) return cudaErrorInvalidValue;
   cudaError_t e;
   // stages: as many as shared memory allows at the variant's CTAs per SM
   if (dh == 64) {
