@@ -257,7 +257,9 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(VerifyArgs a)
         // chunk masses; lane l owns a contiguous block of chunks
         const int cpl = (a.nch + 31) / 32;
         const int c0 = lane * cpl, c1 = min(a.nch, c0 + cpl);
-        double lane_mass = 0.0;
+        // float throughout: this part's fp64 pipe is a small fraction of its
+        // fp32 rate, and a serial fp64 running sum set the walk's time
+        float lane_mass = 0.f;
         for (int c = c0; c < c1; ++c) {
           const ChunkStat st = cs[c];
           float w = st.m > -INFINITY ? st.s * ex2_approx(fmaf(st.m, kLog2e, -mL)) : 0.f;
@@ -267,25 +269,25 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(VerifyArgs a)
           }
           lane_mass += fmaxf(w, 0.f);
         }
-        double incl = lane_mass;
+        float incl = lane_mass;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-          const double v = __shfl_up_sync(0xffffffffu, incl, o);
+          const float v = __shfl_up_sync(0xffffffffu, incl, o);
           if (lane >= o) incl += v;
         }
-        const double excl = incl - lane_mass;
-        const double tgt = static_cast<double>(target);
+        const float excl = incl - lane_mass;
+        const float tgt = target;
         // first lane whose inclusive prefix exceeds the target (else the last lane with mass)
-        unsigned hitb = __ballot_sync(0xffffffffu, incl > tgt && lane_mass > 0.0);
-        unsigned nz = __ballot_sync(0xffffffffu, lane_mass > 0.0);
+        unsigned hitb = __ballot_sync(0xffffffffu, incl > tgt && lane_mass > 0.f);
+        unsigned nz = __ballot_sync(0xffffffffu, lane_mass > 0.f);
         const int hl = hitb ? __ffs(hitb) - 1 : (nz ? 31 - __clz(nz) : 0);
         // the owning lane finds the chunk
         int chunk = -1;
-        double before = 0.0;
+        float before = 0.f;
         if (lane == hl) {
-          double run = excl;
+          float run = excl;
           int lastnz = -1;
-          double lastbefore = excl;
+          float lastbefore = excl;
           for (int c = c0; c < c1; ++c) {
             const ChunkStat st = cs[c];
             float w = st.m > -INFINITY ? st.s * ex2_approx(fmaf(st.m, kLog2e, -mL)) : 0.f;
@@ -332,20 +334,20 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(VerifyArgs a)
               if (!((rejm >> (q * VEC + e)) & 1ull)) lane_w += ex2_approx(fmaf(x[e], sc, -mL));
           }
         }
-        double lincl = lane_w;
+        float lincl = lane_w;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-          const double vv = __shfl_up_sync(0xffffffffu, lincl, o);
+          const float vv = __shfl_up_sync(0xffffffffu, lincl, o);
           if (lane >= o) lincl += vv;
         }
-        const double lexcl = before + (lincl - lane_w);
+        const float lexcl = before + (lincl - lane_w);
         lincl += before;
         hitb = __ballot_sync(0xffffffffu, lincl > tgt && lane_w > 0.f);
         nz = __ballot_sync(0xffffffffu, lane_w > 0.f);
         const int hl2 = hitb ? __ffs(hitb) - 1 : (nz ? 31 - __clz(nz) : 0);
         int tok = -1;
         if (lane == hl2) {
-          double run = lexcl;
+          float run = lexcl;
           int lastnz = -1;
 #pragma unroll
           for (int q = 0; q < NV; ++q) {
