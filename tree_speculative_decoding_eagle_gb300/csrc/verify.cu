@@ -253,85 +253,79 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(VerifyArgs a)
     if (next < 0 || acc >= a.D) {
       if (sample) {
         // ---- bonus: inverse CDF of the residual over the row -------------
-        const float target = s_u[2 * cur + 1] * (Z - rej_sum);
-        // chunk masses; lane l owns a contiguous block of chunks
-        const int cpl = (a.nch + 31) / 32;
-        const int c0 = lane * cpl, c1 = min(a.nch, c0 + cpl);
-        // float throughout: this part's fp64 pipe is a small fraction of its
-        // fp32 rate, and a serial fp64 running sum set the walk's time
-        float lane_mass = 0.f;
-        for (int c = c0; c < c1; ++c) {
+        // Warp-parallel throughout (one lane walking a run of tokens or
+        // chunks with data-dependent branches was the walk's slowest part).
+        // Sums are fp32: this part's fp64 pipe is a small fraction of its
+        // fp32 rate.  A chunk's mass drops its rejected tokens' terms.
+        const float tgt = s_u[2 * cur + 1] * (Z - rej_sum);
+        auto chunk_mass = [&](int c) {
           const ChunkStat st = cs[c];
           float w = st.m > -INFINITY ? st.s * ex2_approx(fmaf(st.m, kLog2e, -mL)) : 0.f;
           for (int q = 0; q < n_rej; ++q) {
             const int t = s_rej[q];
-            if (t >= 0 && t / kChunk == c) w -= s_rej_e[q];
+            w -= (t >= 0 && t / kChunk == c) ? s_rej_e[q] : 0.f;
           }
-          lane_mass += fmaxf(w, 0.f);
-        }
-        float incl = lane_mass;
+          return fmaxf(w, 0.f);
+        };
+        // the chunk: rounds of 32 chunks (lane l takes chunk 32r + l), a
+        // running total carried between rounds; the first chunk whose
+        // inclusive sum exceeds the target, else the last chunk with mass
+        int chunk = -1, last_c = -1;
+        float before = 0.f, last_before = 0.f, carry = 0.f;
+        for (int r0 = 0; r0 < a.nch && chunk < 0; r0 += 32) {
+          const int c = r0 + lane;
+          const float w = c < a.nch ? chunk_mass(c) : 0.f;
+          float incl = w;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float v = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += v;
-        }
-        const float excl = incl - lane_mass;
-        const float tgt = target;
-        // first lane whose inclusive prefix exceeds the target (else the last lane with mass)
-        unsigned hitb = __ballot_sync(0xffffffffu, incl > tgt && lane_mass > 0.f);
-        unsigned nz = __ballot_sync(0xffffffffu, lane_mass > 0.f);
-        const int hl = hitb ? __ffs(hitb) - 1 : (nz ? 31 - __clz(nz) : 0);
-        // the owning lane finds the chunk
-        int chunk = -1;
-        float before = 0.f;
-        if (lane == hl) {
-          float run = excl;
-          int lastnz = -1;
-          float lastbefore = excl;
-          for (int c = c0; c < c1; ++c) {
-            const ChunkStat st = cs[c];
-            float w = st.m > -INFINITY ? st.s * ex2_approx(fmaf(st.m, kLog2e, -mL)) : 0.f;
-            for (int q = 0; q < n_rej; ++q) {
-              const int t = s_rej[q];
-              if (t >= 0 && t / kChunk == c) w -= s_rej_e[q];
-            }
-            w = fmaxf(w, 0.f);
-            if (w > 0.f) { lastnz = c; lastbefore = run; }
-            if (run + w > tgt && w > 0.f) { chunk = c; before = run; break; }
-            run += w;
+          for (int o = 1; o < 32; o <<= 1) {
+            const float v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
           }
-          if (chunk < 0) { chunk = lastnz; before = lastbefore; }
+          const unsigned hit = __ballot_sync(0xffffffffu, w > 0.f && carry + incl > tgt);
+          const unsigned nz = __ballot_sync(0xffffffffu, w > 0.f);
+          if (hit) {
+            const int hl = __ffs(hit) - 1;
+            chunk = r0 + hl;
+            before = carry + __shfl_sync(0xffffffffu, incl - w, hl);
+          } else if (nz) {
+            const int hl = 31 - __clz(nz);
+            last_c = r0 + hl;
+            last_before = carry + __shfl_sync(0xffffffffu, incl - w, hl);
+          }
+          carry += __shfl_sync(0xffffffffu, incl, 31);
         }
-        chunk = __shfl_sync(0xffffffffu, chunk, hl);
-        before = __shfl_sync(0xffffffffu, before, hl);
+        if (chunk < 0) {
+          chunk = last_c;
+          before = last_before;
+        }
         if (chunk < 0) {  // no residual mass anywhere: inputs outside the domain
           bonus = -1;
           break;
         }
-        // scan the chunk: lane l owns 64 consecutive tokens, loaded as
-        // 16-byte vectors into registers; rejected tokens are masked out
+        // the chunk's tokens: lane l owns 64 consecutive tokens; rejected
+        // tokens are masked out
         constexpr int VEC = VecTraits<T>::kElems, NV = 64 / VEC;
         const int tb = chunk * kChunk + lane * 64;
         const int te = min(a.V, tb + 64);
         uint64_t rejm = 0;  // rejected tokens inside [tb, te)
         for (int q = 0; q < n_rej; ++q) {
           const int t = s_rej[q];
-          if (t >= tb && t < te) rejm |= 1ull << (t - tb);
+          rejm |= (t >= tb && t < te) ? 1ull << (t - tb) : 0ull;
         }
         uint4 v[NV];
         const T *rp = reinterpret_cast<const T *>(a.target) + row * a.ld;
 #pragma unroll
         for (int q = 0; q < NV; ++q)
-          if (tb + q * VEC < te) v[q] = *reinterpret_cast<const uint4 *>(rp + tb + q * VEC);
+          v[q] = tb + q * VEC < te ? *reinterpret_cast<const uint4 *>(rp + tb + q * VEC) : make_uint4(0u, 0u, 0u, 0u);
         float lane_w = 0.f;
 #pragma unroll
         for (int q = 0; q < NV; ++q) {
-          if (tb + q * VEC < te) {
-            float x[VEC];
-            VecTraits<T>::unpack(v[q], x);
+          float x[VEC];
+          VecTraits<T>::unpack(v[q], x);
 #pragma unroll
-            for (int e = 0; e < VEC; ++e)
-              if (!((rejm >> (q * VEC + e)) & 1ull)) lane_w += ex2_approx(fmaf(x[e], sc, -mL));
+          for (int e = 0; e < VEC; ++e) {
+            const bool use = tb + q * VEC + e < te && !((rejm >> (q * VEC + e)) & 1ull);
+            lane_w += use ? ex2_approx(fmaf(x[e], sc, -mL)) : 0.f;
           }
         }
         float lincl = lane_w;
@@ -340,33 +334,38 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(VerifyArgs a)
           const float vv = __shfl_up_sync(0xffffffffu, lincl, o);
           if (lane >= o) lincl += vv;
         }
-        const float lexcl = before + (lincl - lane_w);
-        lincl += before;
-        hitb = __ballot_sync(0xffffffffu, lincl > tgt && lane_w > 0.f);
-        nz = __ballot_sync(0xffffffffu, lane_w > 0.f);
-        const int hl2 = hitb ? __ffs(hitb) - 1 : (nz ? 31 - __clz(nz) : 0);
-        int tok = -1;
-        if (lane == hl2) {
-          float run = lexcl;
-          int lastnz = -1;
+        unsigned hitb = __ballot_sync(0xffffffffu, lane_w > 0.f && before + lincl > tgt);
+        const unsigned nzb = __ballot_sync(0xffffffffu, lane_w > 0.f);
+        const bool past_end = hitb == 0;  // rounding: the last token with mass
+        const int hl2 = !past_end ? __ffs(hitb) - 1 : (nzb ? 31 - __clz(nzb) : 0);
+        // the owning lane's 64 tokens, two per lane, read again (L2), with
+        // its rejected-token mask and the mass before them
+        const uint64_t orej = __shfl_sync(0xffffffffu, rejm, hl2);
+        const float obefore = before + __shfl_sync(0xffffffffu, lincl - lane_w, hl2);
+        const int ob = chunk * kChunk + hl2 * 64, oe = min(a.V, ob + 64);
+        const int t0 = ob + 2 * lane, t1 = t0 + 1;
+        float w0 = 0.f, w1 = 0.f;
+        if (t0 < oe && !((orej >> (2 * lane)) & 1ull)) w0 = ex2_approx(fmaf(VecTraits<T>::load1(a.target, row * a.ld + t0), sc, -mL));
+        if (t1 < oe && !((orej >> (2 * lane + 1)) & 1ull)) w1 = ex2_approx(fmaf(VecTraits<T>::load1(a.target, row * a.ld + t1), sc, -mL));
+        float pincl = w0 + w1;
 #pragma unroll
-          for (int q = 0; q < NV; ++q) {
-            if (tok < 0 && tb + q * VEC < te) {
-              float x[VEC];
-              VecTraits<T>::unpack(v[q], x);
-#pragma unroll
-              for (int e = 0; e < VEC; ++e) {
-                if (tok >= 0 || ((rejm >> (q * VEC + e)) & 1ull)) continue;
-                const float w = ex2_approx(fmaf(x[e], sc, -mL));
-                if (w > 0.f) lastnz = tb + q * VEC + e;
-                run += w;
-                if (run > tgt && w > 0.f) tok = tb + q * VEC + e;
-              }
-            }
-          }
-          if (tok < 0) tok = lastnz;
+        for (int o = 1; o < 32; o <<= 1) {
+          const float vv = __shfl_up_sync(0xffffffffu, pincl, o);
+          if (lane >= o) pincl += vv;
         }
-        bonus = __shfl_sync(0xffffffffu, tok, hl2);
+        const float r0 = obefore + (pincl - w0 - w1) + w0, r1 = r0 + w1;
+        const bool h0 = w0 > 0.f && r0 > tgt, h1 = w1 > 0.f && r1 > tgt;
+        const unsigned ph = __ballot_sync(0xffffffffu, !past_end && (h0 || h1));
+        const unsigned pz = __ballot_sync(0xffffffffu, w0 > 0.f || w1 > 0.f);
+        int tok = -1;
+        if (ph) {
+          const int l = __ffs(ph) - 1;
+          tok = __shfl_sync(0xffffffffu, h0 ? t0 : t1, l);
+        } else if (pz) {
+          const int l = 31 - __clz(pz);
+          tok = __shfl_sync(0xffffffffu, w1 > 0.f ? t1 : t0, l);
+        }
+        bonus = tok;
       }
       break;
     }
