@@ -216,9 +216,11 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(VerifyArgs a)
       }
       Z = warp_sum(z);
       for (int base = 0; base < n && next < 0; base += 32) {
-        // the children among nodes base..base+31: each lane takes its
-        // child's logit and uniform, then the decisions are taken in node
-        // order from registers
+        // the children among nodes base..base+31, in node order: every child
+        // before the accepted one was rejected, so child j sees the residual
+        // mass Z - rej_sum - (sum of e over the earlier children here), and
+        // the accepted child is the first whose test passes (one scan, no
+        // serial loop)
         const int i = base + lane;
         const bool kid = i < n && s_par[i] == cur;
         int t_l = -1;
@@ -229,24 +231,25 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(VerifyArgs a)
           else report(a.status, EAGLE_ERR_INVALID);
           u_l = s_u[2 * i];
         }
-        unsigned bal = __ballot_sync(0xffffffffu, kid);
-        while (bal && next < 0) {
-          const int src = __ffs(bal) - 1;
-          bal &= bal - 1;
-          const float e = __shfl_sync(0xffffffffu, e_l, src);
-          const float u0 = __shfl_sync(0xffffffffu, u_l, src);
-          const int t = __shfl_sync(0xffffffffu, t_l, src);
-          if (u0 * (Z - rej_sum) < e) {
-            next = base + src;
-          } else {
-            rej_sum += e;
-            if (lane == 0) {
-              s_rej[n_rej] = (t >= 0 && t < a.V) ? t : -1;
-              s_rej_e[n_rej] = e;
-            }
-            ++n_rej;
-          }
+        float incl = e_l;  // e_l is 0 off the children
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
         }
+        const float excl = incl - e_l;
+        const unsigned kids = __ballot_sync(0xffffffffu, kid);
+        const unsigned acc_b = __ballot_sync(0xffffffffu, kid && u_l * (Z - rej_sum - excl) < e_l);
+        const int first = acc_b ? __ffs(acc_b) - 1 : 32;  // the accepted child's lane
+        const unsigned before = first < 32 ? kids & ((1u << first) - 1u) : kids;  // rejected children
+        if ((before >> lane) & 1u) {
+          const int pos = n_rej + __popc(before & ((1u << lane) - 1u));
+          s_rej[pos] = (t_l >= 0 && t_l < a.V) ? t_l : -1;
+          s_rej_e[pos] = e_l;
+        }
+        n_rej += __popc(before);
+        rej_sum += __shfl_sync(0xffffffffu, first < 32 ? excl : incl, first < 32 ? first : 31);
+        if (first < 32) next = base + first;
       }
       __syncwarp();
     }
