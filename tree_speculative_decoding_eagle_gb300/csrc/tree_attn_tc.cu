@@ -60,10 +60,9 @@ struct TcArgs {
   float *lse;
   int q_tma;          // 1: Q tiles arrive by TMA (G divides the region's rows), else plain loads
   int32_t *status;
-  // KV split through the workspace (part != nullptr): one slot per CTA,
-  // [slot_rows][DH] fp32 O rows then [slot_rows] (m, l) pairs, the slots of
-  // a cluster consecutive.  Otherwise the split merges through distributed
-  // shared memory.
+  // KV split (S > 1) through the workspace: one slot per CTA, [slot_rows][DH]
+  // fp32 O rows then [slot_rows] (m, l) pairs, the slots of a (b, g,
+  // M-group) consecutive.
   float *part;
   int slot_rows;
 };
@@ -146,6 +145,9 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
   const int split = blockIdx.x, mg = blockIdx.y;
   const int bg = blockIdx.z, b = bg / a.Hkv, g = bg % a.Hkv;
   const int n = a.n;
+  const int producer_warp = MT * 4, mma_warp = MT * 4 + 1;
+
+  pdl_wait();  // inputs of this step (kv_len, queries, tree K/V, mask) come from earlier kernels
   const int L = min(max(a.kv_len[b], 0), a.Lmax);
   const int n_ptiles = (L + NK - 1) / NK;
   const int tps = (n_ptiles + a.S - 1) / a.S;
@@ -153,9 +155,6 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
   const int np = p1 - p0;
   const int ntt = (split == a.S - 1) ? (n + NK - 1) / NK : 0;
   const int T = np + ntt;  // key tiles of this CTA
-  const int producer_warp = MT * 4, mma_warp = MT * 4 + 1;
-
-  pdl_wait();  // inputs of this step (queries, tree K/V, mask) come from earlier kernels
   // ---- Q tiles -> shared memory ---------------------------------------------
   // By TMA when the group size divides 128: a box of (64 columns, G heads,
   // 128/G nodes) lands as 128 rows in (node, grouped head) order, the M-tile
