@@ -31,7 +31,11 @@ This walk is exactly lossless (each emitted token has the target's law).
 
 Ambiguity: when a decision's two sides are within `band * Z` of each other,
 fp32 and fp64 evaluations may legitimately disagree; the first such decision
-is reported so a comparison can stop there.
+is reported so a comparison can stop there.  When that decision is the
+bonus draw, the path before it is settled, and the tokens the draw may
+legitimately give are listed: every token with mass whose cumulative
+interval comes within `band * Z` of the draw's threshold (a rounding of the
+running sums by less than the band can move the threshold into any of them).
 """
 from dataclasses import dataclass, field
 
@@ -44,6 +48,7 @@ class WalkResult:
     path: list               # node indices, root first
     tokens: list             # accepted tokens followed by the bonus token
     ambiguous: object = None  # None, or (path position, kind, detail)
+    bonus_choices: tuple = None  # first flag at the bonus draw: the tokens it may give
 
 
 def residual_mass(Z, e, rejected):
@@ -108,10 +113,14 @@ def verify_sample(logits, node_tok, node_parent, temperature, u, band=1e-5):
     hit = np.nonzero(cdf > target)[0]
     bonus = int(hit[0]) if hit.size else int(np.nonzero(w > 0)[0][-1])
     lo = cdf[bonus - 1] if bonus > 0 else 0.0
+    choices = None
     if ambiguous is None and min(abs(target - lo), abs(cdf[bonus] - target)) <= band * Z:
         ambiguous = (len(path) - 1, "bonus", bonus)
+        below = np.concatenate(([0.0], cdf[:-1]))   # each token's interval [below, cdf)
+        near = (w > 0) & (cdf > target - band * Z) & (below <= target + band * Z)
+        choices = tuple(int(v) for v in np.nonzero(near)[0])
     tokens = [int(node_tok[p]) for p in path[1:]] + [bonus]
-    return WalkResult(len(path) - 1, path, tokens, ambiguous)
+    return WalkResult(len(path) - 1, path, tokens, ambiguous, choices)
 
 
 def verify(logits, node_tok, node_parent, D, mode, temperature=1.0, u=None):

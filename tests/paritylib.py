@@ -117,21 +117,38 @@ def attn_expected(case, ai_cpu, masks_bool):
     return res
 
 
+def check_walk(mode, acc_g, path_g, tok_g, acc_o, path_o, tok_o, r):
+    """One sequence.  Greedy, and sampling without a flagged decision: exact.
+    First flag at the bonus draw: path, accepted length and accepted tokens
+    exact, the bonus one of the oracle's admissible tokens.  First flag at an
+    accept test (two sides within 1e-5 of the row mass): exact up to that
+    node.  Returns True when the comparison stopped at an accept test."""
+    if mode == "greedy" or r.ambiguous is None:
+        assert acc_g == acc_o, (acc_g, acc_o)
+        assert (path_g == path_o).all()
+        assert (tok_g == tok_o).all()
+        return False
+    pos = r.ambiguous[0]
+    if r.ambiguous[1] == "bonus":
+        assert acc_g == acc_o, (acc_g, acc_o)
+        assert (path_g == path_o).all()
+        assert (tok_g[:acc_o] == tok_o[:acc_o]).all()
+        assert int(tok_g[acc_o]) in r.bonus_choices, (int(tok_g[acc_o]), r.bonus_choices)
+        return False
+    assert (path_g[:pos + 1] == path_o[:pos + 1]).all()
+    return True
+
+
 def compare_walk(w, mode, acc_g, path_g, tok_g, want, seqs):
-    """Greedy: exact.  Sampling: exact up to the oracle's first ambiguous
-    decision (two sides within 1e-5 of the row mass)."""
+    """Every sequence by check_walk; returns how many stopped at a flagged
+    accept test."""
     acc_o, path_o, tok_o, walks = want
     n_amb = 0
     for b in seqs:
-        r = walks[b]
-        if mode == "greedy" or r.ambiguous is None:
-            assert acc_g[b] == acc_o[b], (b, acc_g[b], acc_o[b])
-            assert (path_g[b] == path_o[b]).all(), b
-            assert (tok_g[b] == tok_o[b]).all(), b
-        else:
-            n_amb += 1
-            pos = r.ambiguous[0]
-            assert (path_g[b, :pos + 1] == path_o[b, :pos + 1]).all(), b
+        try:
+            n_amb += check_walk(mode, acc_g[b], path_g[b], tok_g[b], acc_o[b], path_o[b], tok_o[b], walks[b])
+        except AssertionError as e:
+            raise AssertionError(f"sequence {b}: {e}") from e
     return n_amb
 
 

@@ -166,8 +166,10 @@ def run_case(case):
             acc_o[b] = r.accept_len
             path_o[b, :len(r.path)] = r.path
             tok_ow[b, :len(r.tokens)] = r.tokens
+        # an accept test is flagged with probability about 2e-5 Z / R (R the
+        # residual mass), so over a case's few hundred tests at most one is
         n_amb = compare_walk(w, mode, acc, path, toks, (acc_o, path_o, tok_ow, walks), seqs)
-        assert n_amb <= max(1, len(seqs) // 4)
+        assert n_amb <= 1
         taus[mode] = float(np.mean([acc_o[b] for b in seqs]))
     return taus
 

@@ -86,7 +86,7 @@ def test_sampled_drafts_match_oracle(name):
     target = gen.target_logits(w, draft, row)
     u = gen.uniforms(w)
     n_amb, acc_o = run_and_compare(w, draft, target, tok, par, row, c["T"], u)
-    assert n_amb <= max(1, w.B // 3)
+    assert n_amb <= 1  # flagged walks are rare: none of these cases has one
 
 
 def test_dynamic_tree_top_k_drafts():

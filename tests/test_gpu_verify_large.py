@@ -15,6 +15,7 @@ import torch
 
 import tree_speculative_decoding_eagle_gb300 as eg
 from oracle import verify as over
+from paritylib import check_walk
 
 pytestmark = pytest.mark.gpu
 
@@ -67,15 +68,9 @@ def test_verify_large_tree(m, mode):
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     acc, path, toks = acc.cpu().numpy(), path.cpu().numpy(), toks.cpu().numpy()
-    checked = 0
-    for b in range(B):
-        if mode == "sample" and walks[b].ambiguous is not None:
-            continue
-        assert acc[b] == acc_o[b], b
-        assert (path[b] == path_o[b]).all(), b
-        assert (toks[b] == tok_o[b]).all(), b
-        checked += 1
-    assert checked >= 1
+    stopped = sum(check_walk(mode, acc[b], path[b], toks[b], acc_o[b], path_o[b], tok_o[b], walks[b])
+                  for b in range(B))
+    assert stopped <= 1
     assert acc_o.max() >= 1          # the planted paths make walks take steps
 
 

@@ -146,6 +146,43 @@ def test_ambiguity_is_flagged_at_the_boundary():
     assert r.ambiguous is not None and r.ambiguous[1] == "accept"
 
 
+def test_bonus_on_a_boundary_lists_both_neighbours():
+    # root only, p = (1/2, 1/4, 1/4): u = 1/2 puts the threshold exactly on
+    # the boundary between tokens 0 and 1; the draw takes token 1 (the first
+    # cumulative sum above the threshold) and either is admissible
+    logits = np.log(np.array([[0.5, 0.25, 0.25]]))
+    r = over.verify_sample(logits, [-1], [-1], 1.0, np.array([[0.0, 0.5]]))
+    assert r.tokens == [1]
+    assert r.ambiguous is not None and r.ambiguous[1] == "bonus"
+    assert r.bonus_choices == (0, 1)
+
+
+def test_bonus_choices_include_a_token_lighter_than_the_band():
+    # token 1 carries 1e-7 of the mass, less than the band: a threshold at
+    # its interval may land in token 0, 1 or 2 under rounding
+    p = np.array([0.5, 1e-7, 0.5 - 1e-7])
+    r = over.verify_sample(np.log(p)[None], [-1], [-1], 1.0, np.array([[0.0, 0.5 + 5e-8]]))
+    assert r.tokens == [1]
+    assert r.bonus_choices == (0, 1, 2)
+
+
+def test_bonus_choices_skip_rejected_tokens():
+    # the root's child (token 0) is rejected, so the draw is over tokens 1, 2
+    # only; u = 1/2 of the residual 1/2 puts the threshold on their boundary
+    logits = np.log(np.array([[0.5, 0.25, 0.25], [1 / 3, 1 / 3, 1 / 3]]))
+    u = np.array([[0.0, 0.5], [0.999, 0.0]])
+    r = over.verify_sample(logits, [-1, 0], [-1, 0], 1.0, u)
+    assert r.accept_len == 0 and r.tokens == [2]
+    assert r.bonus_choices == (1, 2)
+
+
+def test_no_flag_no_choices(golden_dir):
+    with open(os.path.join(golden_dir, "hand_sample.json")) as f:
+        h = json.load(f)
+    r = over.verify_sample(np.log(np.array(h["probs"])), h["node_tok"], h["node_parent"], 1.0, np.array(h["u"]))
+    assert r.ambiguous is None and r.bonus_choices is None
+
+
 def test_planted_unremoved_mass_fails_monte_carlo(monkeypatch):
     monkeypatch.setattr(over, "residual_mass", lambda Z, e, rejected: Z)
     p, first, _, _ = mc_run(20000, 1.0, seed=13)
