@@ -9,6 +9,7 @@
  *   eagle_tree_mask   ancestor-only attention mask from parent pointers
  *   eagle_tree_attn   tree-masked attention of the tree nodes over the KV prefix
  *   eagle_verify      greedy or speculative-sampling verification walk
+ * and eagle_step runs the four in order (or replays them as one graph).
  *
  * Sources (the pages the method is taken from):
  *   [EAGLE-2] "論文解説: EAGLE-2 - 動的ドラフトツリーによるLLM推論の高速化"
@@ -462,6 +463,95 @@ int eagle_kv_commit(const void *k_tree, const void *v_tree, int dtype, int B,
                     int max_pages, int page_size, int num_pages,
                     int32_t *kv_len, int32_t *slot_mapping, int32_t *status,
                     eagle_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * The whole step in one call, and as one recorded graph.
+ * [EAGLE-2] section "動的ドラフトツリーの構築アルゴリズム" (draft confidences,
+ * then the tree), [EAGLE-1] sections "Tree Attention の役割" (the target
+ * scores the tree in one pass) and "検証方法" (then verification): the
+ * stages run in that order, each on the previous one's results:
+ *   eagle_draft_topk -> eagle_tree_build (with the mask) -> eagle_tree_attn
+ *   -> eagle_verify
+ * on one stream, each kernel chained to the previous one.  The target
+ * logits are an input: the target's layers between the attention and its
+ * logits are not part of the library.
+ *
+ * eagle_step_args names every buffer of the four calls; each field means
+ * what the argument of the same name means there (n = m + 1 tree nodes):
+ *   draft_logits, draft_ld            eagle_draft_topk's logits, ld
+ *   tok, conf, stats                  its outputs (stats may be NULL)
+ *   root_tok, node_tok ... node_row   eagle_tree_build's (root_tok,
+ *                                     node_depth, node_score, node_src and
+ *                                     node_row may be NULL)
+ *   mask                              required: the attention reads it
+ *   q, k_cache, v_cache, kv_len, k_tree, v_tree, scale, attn_out, lse
+ *                                     eagle_tree_attn's (attn_out is its
+ *                                     `out`; lse may be NULL)
+ *   target, target_ld, uniforms, accept_len, path_nodes, out_tokens
+ *                                     eagle_verify's (uniforms only for
+ *                                     EAGLE_SAMPLE)
+ *   status                            one word shared by every stage (may
+ *                                     be NULL)
+ * dtype applies to the draft logits, the attention tensors and the target
+ * logits alike.
+ * ------------------------------------------------------------------------ */
+typedef struct eagle_step_args {
+  int dtype;
+  int B, D, k, m, V;
+  int Hq, Hkv, dh, Lmax;
+  int mode;
+  float temperature;
+  float scale;
+  const void *draft_logits;
+  int64_t draft_ld;
+  int32_t *tok;
+  float *conf;
+  float *stats;
+  const int32_t *root_tok;
+  int32_t *node_tok, *node_parent, *node_depth;
+  float *node_score;
+  int32_t *node_src, *node_row;
+  uint64_t *mask;
+  const void *q, *k_cache, *v_cache;
+  const int32_t *kv_len;
+  const void *k_tree, *v_tree;
+  void *attn_out;
+  float *lse;
+  const void *target;
+  int64_t target_ld;
+  const float *uniforms;
+  int32_t *accept_len, *path_nodes, *out_tokens;
+  int32_t *status;
+} eagle_step_args;
+
+/* Bytes of the one workspace a step needs (the stages' workspaces, each at
+ * a 256-byte aligned offset); 0 for invalid arguments.  Host only. */
+size_t eagle_step_workspace_size(const eagle_step_args *args);
+
+/* The four calls in order on `stream`.  Returns the first nonzero status
+ * of a call (the calls after it are not made); the arguments of each call
+ * are checked by that call. */
+int eagle_step(const eagle_step_args *args, void *workspace,
+               size_t workspace_bytes, eagle_stream_t stream);
+
+/* A step recorded once into a CUDA graph; each launch replays all of its
+ * kernels with one call.  The graph holds the buffers' addresses (and the
+ * tensor maps built from them), so every buffer and the workspace must stay
+ * allocated, at the same address, until the graph is destroyed; their
+ * contents (inputs, kv_len) may change between launches.
+ * eagle_step_graph_create first runs the step once on a stream of its own
+ * (work that produces the inputs on other streams must have completed) and
+ * waits for it (one-time kernel set-up happens outside the recording; the
+ * outputs are then those of that run), then records the step on that
+ * stream (capture mode local to the calling thread) and instantiates the
+ * graph.  Unlike the other calls it allocates (the stream and the graph)
+ * and synchronises; the launches do neither.  On failure *graph is NULL. */
+typedef struct eagle_step_graph_s *eagle_step_graph_t;
+
+int eagle_step_graph_create(const eagle_step_args *args, void *workspace,
+                            size_t workspace_bytes, eagle_step_graph_t *graph);
+int eagle_step_graph_launch(eagle_step_graph_t graph, eagle_stream_t stream);
+int eagle_step_graph_destroy(eagle_step_graph_t graph);
 
 #ifdef __cplusplus
 }

@@ -110,3 +110,70 @@ def test_workspace_queries_are_host_only(lib):
     assert lib.eagle_tree_attn_workspace_size(BF16, 64, 61, 64, 8, 64, 8192) == 0
     assert lib.eagle_tree_attn_kernel_count(BF16, 8, 51, 40, 40, 128, 4096) == 2   # several waves: merge kernel
     assert lib.eagle_tree_attn_kernel_count(BF16, 0, 61, 32, 32, 128, 2048) == 0
+
+
+def _step_args(**over):
+    a = eg.StepArgs()
+    vals = dict(dtype=eg.BF16, B=1, D=6, k=10, m=60, V=32000, Hq=32, Hkv=32, dh=128, Lmax=2048,
+                mode=eg.GREEDY, temperature=1.0, scale=128 ** -0.5)
+    vals.update(over)
+    for f, v in vals.items():
+        setattr(a, f, v)
+    return a
+
+
+def test_step_args_layout_matches_the_header(tmp_path):
+    """ctypes' StepArgs and the C struct agree field for field (offsets and
+    size from a C program compiled against include/eagle.h)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    names = [f for f, _ in eg.StepArgs._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "eagle.h"\nint main(void) {\n'
+                   '  printf("%zu\\n", sizeof(eagle_step_args));\n'
+                   + "".join(f'  printf("%zu\\n", offsetof(eagle_step_args, {n}));\n' for n in names)
+                   + "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    out = [int(x) for x in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()]
+    assert out[0] == ctypes.sizeof(eg.StepArgs)
+    assert out[1:] == [getattr(eg.StepArgs, n).offset for n in names]
+
+
+def test_step_workspace_is_the_stages_workspaces(lib):
+    r = lambda x: (x + 255) // 256 * 256
+    a = _step_args()
+    want = (r(lib.eagle_draft_topk_workspace_size(1, 6, 10, 32000))
+            + r(lib.eagle_tree_attn_workspace_size(eg.BF16, 1, 61, 32, 32, 128, 2048))
+            + r(lib.eagle_verify_workspace_size(1, 60, 32000)))
+    assert lib.eagle_step_workspace_size(ctypes.byref(a)) == want > 0
+    assert lib.eagle_step_workspace_size(None) == 0
+    assert lib.eagle_step_workspace_size(ctypes.byref(_step_args(B=0))) == 0
+
+
+def test_step_rejects_on_the_host(lib):
+    fake = 0x1000
+    a = _step_args()
+    for f in ("draft_logits", "tok", "conf", "node_tok", "node_parent", "q", "k_cache", "v_cache", "kv_len",
+              "k_tree", "v_tree", "attn_out", "target", "accept_len", "path_nodes", "out_tokens"):
+        setattr(a, f, fake)
+    a.draft_ld = a.target_ld = 32000
+    need = lib.eagle_step_workspace_size(ctypes.byref(a))
+    ws = ctypes.c_void_p(0x100000)
+    assert lib.eagle_step(None, ws, need, None) == -1
+    assert lib.eagle_step(ctypes.byref(a), ws, need, None) == -1          # no mask: the attention needs it
+    a.mask = fake
+    assert lib.eagle_step(ctypes.byref(a), ws, need - 1, None) == -4      # workspace too small
+    assert lib.eagle_step(ctypes.byref(a), None, need, None) == -4
+    bad = _step_args(k=33)                                                  # stage 1 rejects k > 32
+    for f in ("draft_logits", "tok", "conf", "mask"):
+        setattr(bad, f, fake)
+    bad.draft_ld = 32000
+    nb = lib.eagle_step_workspace_size(ctypes.byref(bad))
+    assert lib.eagle_step(ctypes.byref(bad), ws, nb, None) == -1
+    assert lib.eagle_step_graph_create(ctypes.byref(a), ws, need, None) == -1
+    assert lib.eagle_step_graph_launch(None, None) == -1
+    assert lib.eagle_step_graph_destroy(None) == 0

@@ -18,6 +18,8 @@ library is missing or a call reports an error, an exception is raised.
     verify_noalloc -> eagle_verify_noalloc (the same without a caller workspace)
     verify_draft -> eagle_verify_draft (sampling walk against draft distributions q)
     selftest_wait -> eagle_selftest_wait (a bounded device wait that must give up)
+    step / StepGraph -> eagle_step, eagle_step_graph_* (the four stages in one
+                   call, or recorded once as a graph and replayed)
 """
 import ctypes
 import os
@@ -38,6 +40,8 @@ EXPORTED = (
     "eagle_tree_attn_workspace_size", "eagle_tree_attn_kernel_count", "eagle_tree_attn",
     "eagle_tree_attn_paged_workspace_size", "eagle_tree_attn_paged", "eagle_kv_commit",
     "eagle_verify_workspace_size", "eagle_verify", "eagle_verify_noalloc", "eagle_verify_draft",
+    "eagle_step_workspace_size", "eagle_step", "eagle_step_graph_create", "eagle_step_graph_launch",
+    "eagle_step_graph_destroy",
 )
 
 _lib = None
@@ -45,6 +49,29 @@ _lib = None
 
 class EagleError(RuntimeError):
     pass
+
+
+_P, _I, _I64, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+
+
+class StepArgs(ctypes.Structure):
+    """eagle_step_args: every buffer of the four stage calls (device
+    pointers) and the step's shapes, field for field as include/eagle.h
+    declares them."""
+    _fields_ = [
+        ("dtype", _I), ("B", _I), ("D", _I), ("k", _I), ("m", _I), ("V", _I),
+        ("Hq", _I), ("Hkv", _I), ("dh", _I), ("Lmax", _I),
+        ("mode", _I), ("temperature", _F), ("scale", _F),
+        ("draft_logits", _P), ("draft_ld", _I64),
+        ("tok", _P), ("conf", _P), ("stats", _P),
+        ("root_tok", _P), ("node_tok", _P), ("node_parent", _P), ("node_depth", _P),
+        ("node_score", _P), ("node_src", _P), ("node_row", _P), ("mask", _P),
+        ("q", _P), ("k_cache", _P), ("v_cache", _P), ("kv_len", _P), ("k_tree", _P), ("v_tree", _P),
+        ("attn_out", _P), ("lse", _P),
+        ("target", _P), ("target_ld", _I64), ("uniforms", _P),
+        ("accept_len", _P), ("path_nodes", _P), ("out_tokens", _P),
+        ("status", _P),
+    ]
 
 
 def load_library(path=LIB_PATH):
@@ -76,6 +103,11 @@ def load_library(path=LIB_PATH):
         "eagle_verify": (I, [P, I, I64, P, P, I, I, I, I, I, F, P, P, P, P, P, P, SZ, P]),
         "eagle_verify_noalloc": (I, [P, I, I64, P, P, I, I, I, I, I, F, P, P, P, P, P, P]),
         "eagle_verify_draft": (I, [P, P, I, I64, I64, P, P, P, I, I, I, I, I, F, P, P, P, P, P, P]),
+        "eagle_step_workspace_size": (SZ, [ctypes.POINTER(StepArgs)]),
+        "eagle_step": (I, [ctypes.POINTER(StepArgs), P, SZ, P]),
+        "eagle_step_graph_create": (I, [ctypes.POINTER(StepArgs), P, SZ, ctypes.POINTER(P)]),
+        "eagle_step_graph_launch": (I, [P, P]),
+        "eagle_step_graph_destroy": (I, [P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -372,3 +404,52 @@ def selftest_wait(limit_ns=1_000_000, which=0, stream=None):
            "eagle_selftest_wait")
     (stream or torch.cuda.current_stream()).synchronize()
     return int(status.item()), int(elapsed.item())
+
+
+def step_workspace_size(args):
+    """Bytes of the one workspace eagle_step needs for these arguments."""
+    return load_library().eagle_step_workspace_size(ctypes.byref(args))
+
+
+def step(args, workspace, stream=None):
+    """eagle_step: the four stages in order on the current stream.  `args`
+    is a StepArgs (TreeStep.step_args builds one); `workspace` a Workspace."""
+    lib = load_library()
+    buf, nbytes = workspace.get(lib.eagle_step_workspace_size(ctypes.byref(args)))
+    _check(lib.eagle_step(ctypes.byref(args), _ptr(buf), nbytes, _stream(stream)), "eagle_step")
+
+
+class StepGraph:
+    """eagle_step_graph_*: the step recorded once (after one plain run) and
+    replayed by launch().  The buffers named in `args` and the workspace
+    must stay allocated until close(); their contents may change between
+    launches."""
+
+    def __init__(self, args, workspace):
+        lib = load_library()
+        self._args = args
+        buf, nbytes = workspace.get(lib.eagle_step_workspace_size(ctypes.byref(args)))
+        self._ws = buf
+        # the library's first run is on a stream of its own: the inputs'
+        # producers on this stream must have finished
+        torch.cuda.current_stream().synchronize()
+        handle = ctypes.c_void_p()
+        _check(lib.eagle_step_graph_create(ctypes.byref(args), _ptr(buf), nbytes, ctypes.byref(handle)),
+               "eagle_step_graph_create")
+        self._h = handle
+
+    def launch(self, stream=None):
+        if self._h is None:
+            raise EagleError("the step graph is closed")
+        _check(load_library().eagle_step_graph_launch(self._h, _stream(stream)), "eagle_step_graph_launch")
+
+    def close(self):
+        if self._h is not None:
+            _check(load_library().eagle_step_graph_destroy(self._h), "eagle_step_graph_destroy")
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
