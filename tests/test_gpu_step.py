@@ -64,7 +64,7 @@ def test_one_call_step_and_its_graph_match_the_stage_calls(name):
 
     args = ts.step_args(**inputs)
     ws = eg.Workspace()
-    eg.step(args, ws)
+    eg.run_step(args, ws)
     torch.cuda.synchronize()
     assert_same(outputs(ts), want)
 

@@ -18,8 +18,8 @@ library is missing or a call reports an error, an exception is raised.
     verify_noalloc -> eagle_verify_noalloc (the same without a caller workspace)
     verify_draft -> eagle_verify_draft (sampling walk against draft distributions q)
     selftest_wait -> eagle_selftest_wait (a bounded device wait that must give up)
-    step / StepGraph -> eagle_step, eagle_step_graph_* (the four stages in one
-                   call, or recorded once as a graph and replayed)
+    run_step / StepGraph -> eagle_step, eagle_step_graph_* (the four stages
+                   in one call, or recorded once as a graph and replayed)
 """
 import ctypes
 import os
@@ -411,7 +411,7 @@ def step_workspace_size(args):
     return load_library().eagle_step_workspace_size(ctypes.byref(args))
 
 
-def step(args, workspace, stream=None):
+def run_step(args, workspace, stream=None):
     """eagle_step: the four stages in order on the current stream.  `args`
     is a StepArgs (TreeStep.step_args builds one); `workspace` a Workspace."""
     lib = load_library()
