@@ -214,6 +214,12 @@ inline cudaError_t set_smem_limit_max_once(Kernel kernel, std::atomic<unsigned l
 // for a kernel launched the ordinary way.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Requests the line holding p into L2 without reading it into the SM: safe
+// before pdl_wait() (L2 is coherent for the whole device, so a later load
+// after the wait still sees the previous kernel's writes).
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)) : "memory");
+}
 
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_chained(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,

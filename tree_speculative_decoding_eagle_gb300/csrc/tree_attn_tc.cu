@@ -147,6 +147,7 @@ __global__ void __launch_bounds__(MT * 128 + 64, MT == 1 ? 2 : 1)
   const int n = a.n;
   const int producer_warp = MT * 4, mma_warp = MT * 4 + 1;
 
+  if (tid == 0) prefetch_l2(a.kv_len + b);  // its load below then waits on L2, not DRAM
   pdl_wait();  // inputs of this step (kv_len, queries, tree K/V, mask) come from earlier kernels
   const int L = min(max(a.kv_len[b], 0), a.Lmax);
   const int n_ptiles = (L + NK - 1) / NK;
