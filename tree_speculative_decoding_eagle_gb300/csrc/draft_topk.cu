@@ -258,12 +258,14 @@ __global__ void __launch_bounds__(NW * 32, NW <= 8 ? 3 : 1) draft_topk_kernel(Dr
   float M = -INFINITY, Z = 0.f;  // the part's softmax statistics (warp 0)
   if constexpr (NW == 16) {
     // ---- one segment per warp: selection against one block-wide bound ----
-    // Warp w has k distinct elements (lane maxima) at or above its k-th
-    // largest lane maximum, so the largest of these over the warps, T,
-    // bounds the part's k-th largest value from below.  Every element at or
-    // above T is gathered (one shared atomic per warp) and the gathered keys
-    // are ranked by counting.  A flat row with more than kGatherCap such
-    // elements takes the per-warp lists instead.
+    // The k-th largest of the warps' maxima, T: the warps whose maximum is
+    // at or above T are at least k, each with a distinct element there, so
+    // T bounds the part's k-th largest value from below.  (When fewer than
+    // k warps hold a segment, T is the largest over the warps of each
+    // warp's k-th largest lane maximum, a bound for the same reason.)  Every
+    // element at or above T is gathered (one shared atomic per warp) and the
+    // gathered keys are ranked by counting.  A flat row with more than
+    // kGatherCap such elements takes the per-warp lists instead.
     constexpr int kGatherCap = 256;
     const int gseg = g0 + warp;
     const bool has = gseg < g1;  // warp-uniform
@@ -276,7 +278,8 @@ __global__ void __launch_bounds__(NW * 32, NW <= 8 ? 3 : 1) draft_topk_kernel(Dr
       vmx[i] = (lane + 32 * i < nvec) ? vec_max<T>(vb[i]) : -INFINITY;
       smax = fmaxf(smax, vmx[i]);
     }
-    if (has) {
+    const bool by_warps = k <= g1 - g0;  // at least k warps hold a segment (block-uniform)
+    if (has && !by_warps) {
       const float y = warp_sort_desc(smax, lane);
       const float kth = __shfl_sync(0xffffffffu, y, k - 1);
       if (lane == 0 && kth > -INFINITY) atomicMax(&s_thr, ordered_u32(kth));
@@ -295,7 +298,19 @@ __global__ void __launch_bounds__(NW * 32, NW <= 8 ? 3 : 1) draft_topk_kernel(Dr
       }
     }
     __syncthreads();
-    const float bound = from_ordered_u32(s_thr);
+    float bound = from_ordered_u32(s_thr);
+    if (by_warps) {
+      // the warp maximum of rank k-1 (greater, or equal at a lower warp, ranks first)
+      const float wm = lane < NW ? s_m[lane] : -INFINITY;
+      int rk = 0;
+#pragma unroll
+      for (int j = 0; j < NW; ++j) {
+        const float o = s_m[j];
+        rk += (o > wm) || (o == wm && j < lane);
+      }
+      const unsigned at = __ballot_sync(0xffffffffu, lane < NW && rk == k - 1 && wm > -INFINITY);
+      if (at) bound = fmaxf(bound, __shfl_sync(0xffffffffu, wm, __ffs(at) - 1));
+    }
     unsigned cms[NVL];
     int mycnt = 0;
 #pragma unroll
