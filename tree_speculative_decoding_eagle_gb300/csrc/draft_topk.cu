@@ -7,8 +7,9 @@
 //
 // One pass over HBM.  A row is split into S <= 8 parts, one CTA each; the
 // parts of a row form one thread-block cluster.  Few rows (each part fits
-// one segment per warp with the parts of all rows resident at once) take
-// 16-warp CTAs with 1024-token segments, held in registers (all 16-byte
+// one segment per warp, and the parts of all rows fit three waves of two
+// CTAs per SM) take 16-warp CTAs with 1024-token segments, held in
+// registers (all 16-byte
 // loads in flight at once); many rows take 8-warp CTAs, three per SM, whose
 // warps stream 1024-token segments through a three-stage ring in shared
 // memory (asynchronous copies issued two segments ahead, so the loads stay
@@ -135,7 +136,7 @@ __device__ __forceinline__ float segment_exp_sum(const uint4 (&vb)[NVL], int nve
 
 // NW warps per CTA, NVL 16-byte vectors per lane and segment.
 template <typename T, int NW, int NVL>
-__global__ void __launch_bounds__(NW * 32, NW <= 8 ? 3 : 1) draft_topk_kernel(DraftArgs a) {
+__global__ void __launch_bounds__(NW * 32, NW <= 8 ? 3 : 2) draft_topk_kernel(DraftArgs a) {
   using VT = VecTraits<T>;
   constexpr int VEC = VT::kElems;
   constexpr int SEG = 32 * NVL * VEC;  // tokens per warp and segment
@@ -670,8 +671,8 @@ struct DraftPlan {
 };
 
 // Few rows: 16-warp CTAs with 1024-token segments (bf16), when each row can
-// be split into parts of one segment per warp with every part resident at
-// once (one CTA per SM).  Otherwise 8-warp CTAs streaming 1024-token
+// be split into parts of one segment per warp and the parts take at most
+// three waves of two CTAs per SM.  Otherwise 8-warp CTAs streaming 1024-token
 // segments through a shared-memory ring: enough parts for about three CTAs
 // per SM, but no part smaller than one segment per warp.  At most
 // kMaxDraftParts parts per row (one cluster).
@@ -682,7 +683,7 @@ static DraftPlan draft_plan(int B, int R, int V, int vec, int num_sms) {
     const int seg = 4 * 32 * vec;
     const int64_t nseg = (V + seg - 1) / seg;
     const int64_t parts = (nseg + 15) / 16;
-    if (parts <= kMaxDraftParts && rows * parts <= num_sms) {
+    if (parts <= kMaxDraftParts && rows * parts <= 6 * static_cast<int64_t>(num_sms)) {
       p.NW = 16;
       p.NVL = 4;
       p.S = static_cast<int>(parts);
