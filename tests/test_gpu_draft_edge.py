@@ -5,11 +5,12 @@ a handful of levels, and ordinary rows.  Tokens must equal the oracle's
 (ties -> lower token id), confidences and log-sums within the parity
 tolerances.
 
-Shapes cover both launch forms: one sequence of Llama-2-7B-shaped rows
-(few rows: 16-warp CTAs, each row split over a cluster of CTAs) and four
-sequences (8-warp CTAs), in bf16 and fp32, plus k = 32 (also with every
-row split over an 8-CTA cluster), and many short rows whose 8-warp CTAs
-have fewer segments than warps or a one-vector last segment.
+Shapes cover both launch forms: Llama-2-7B-shaped rows for one sequence
+and for four (16-warp CTAs, each row split over a cluster of CTAs; four
+sequences take several waves of them) and for twenty (8-warp CTAs streaming
+through the shared-memory ring), in bf16 and fp32, plus k = 32 (also with
+every row split over an 8-CTA cluster), and short rows with a one-vector
+last segment in both forms, or fewer segments than warps in the ring form.
 """
 import numpy as np
 import pytest
@@ -50,18 +51,22 @@ def edge_rows(B, D, k, V, seed):
 
 
 CASES = [
+    # 16-warp CTAs, one segment per warp (one wave, or several of two CTAs per SM):
     ("bf16", 1, 6, 10, 32000),
-    ("bf16", 4, 6, 10, 32000),
+    ("bf16", 4, 6, 10, 32000),      # 408 CTAs: two waves
     ("f32", 1, 6, 10, 32000),
     ("f32", 4, 6, 10, 32000),
     ("bf16", 1, 3, 32, 4096),
+    ("bf16", 16, 6, 10, 4104),      # a last segment of one 16-byte vector
+    ("f32", 32, 4, 8, 1028),        # fp32 segments of 512 tokens, a one-vector tail
+    # 8-warp CTAs streaming segments through the shared-memory ring:
     ("bf16", 2, 2, 4, 201088),
     ("bf16", 1, 2, 32, 201088),     # 8-part clusters with k = 32: the part merge ranks 256 keys
-    # 8-warp CTAs streaming segments through the shared-memory ring:
+    ("bf16", 20, 6, 10, 32000),     # 1020 rows of 32 segments: four per warp
     ("bf16", 64, 6, 10, 4096),      # four segments per row: half the warps have none, the ring's
                                     # look-ahead stages are empty copy groups
-    ("bf16", 16, 6, 10, 4104),      # a last segment of one 16-byte vector (lane 0 alone copies)
-    ("f32", 32, 4, 8, 1028),        # fp32 segments of 512 tokens, a one-vector tail
+    ("bf16", 24, 6, 10, 4104),      # a last segment of one 16-byte vector (lane 0 alone copies)
+    ("f32", 40, 4, 8, 1028),        # fp32 segments of 512 tokens, a one-vector tail
 ]
 
 
