@@ -5,12 +5,14 @@ a handful of levels, and ordinary rows.  Tokens must equal the oracle's
 (ties -> lower token id), confidences and log-sums within the parity
 tolerances.
 
-Shapes cover both launch forms: Llama-2-7B-shaped rows for one sequence
-and for four (16-warp CTAs, each row split over a cluster of CTAs; four
-sequences take several waves of them) and for twenty (8-warp CTAs streaming
-through the shared-memory ring), in bf16 and fp32, plus k = 32 (also with
-every row split over an 8-CTA cluster), and short rows with a one-vector
-last segment in both forms, or fewer segments than warps in the ring form.
+Shapes cover the three launch forms, in bf16 and fp32: 16-warp CTAs with
+one segment per warp (Llama-2-7B-shaped rows for one sequence and, in two
+waves, for four; k = 32 with every row split over an 8-CTA cluster; short
+rows with a one-vector last segment or fewer segments than k); 4-warp ring
+CTAs (rows with fewer than eight segments per warp of an 8-warp CTA:
+clusters of 6 parts with k = 32, 1020 rows of 32 segments, rows with fewer
+segments than warps, one-vector tails); and 8-warp ring CTAs (rows of 64
+and 65 segments, with k = 10 and k = 32).
 """
 import numpy as np
 import pytest
@@ -57,16 +59,22 @@ CASES = [
     ("f32", 1, 6, 10, 32000),
     ("f32", 4, 6, 10, 32000),
     ("bf16", 1, 3, 32, 4096),
+    ("bf16", 1, 2, 32, 131072),     # 8-part clusters with k = 32: the part merge ranks 256 keys
     ("bf16", 16, 6, 10, 4104),      # a last segment of one 16-byte vector
     ("f32", 32, 4, 8, 1028),        # fp32 segments of 512 tokens, a one-vector tail
-    # 8-warp CTAs streaming segments through the shared-memory ring:
+    # 4-warp CTAs streaming segments through the shared-memory ring:
     ("bf16", 2, 2, 4, 201088),
-    ("bf16", 1, 2, 32, 201088),     # 8-part clusters with k = 32: the part merge ranks 256 keys
-    ("bf16", 20, 6, 10, 32000),     # 1020 rows of 32 segments: four per warp
-    ("bf16", 64, 6, 10, 4096),      # four segments per row: half the warps have none, the ring's
-                                    # look-ahead stages are empty copy groups
+    ("bf16", 1, 2, 32, 201088),     # 6-part clusters with k = 32
+    ("bf16", 20, 6, 10, 32000),     # 1020 rows of 32 segments: eight per warp
+    ("bf16", 64, 6, 10, 4096),      # four segments per row, one per warp: the ring's look-ahead
+                                    # stages are empty copy groups
     ("bf16", 24, 6, 10, 4104),      # a last segment of one 16-byte vector (lane 0 alone copies)
-    ("f32", 40, 4, 8, 1028),        # fp32 segments of 512 tokens, a one-vector tail
+    ("f32", 40, 4, 8, 1028),        # fp32 segments of 512 tokens, a one-vector tail, a warp with none
+    # 8-warp CTAs streaming segments through the shared-memory ring:
+    ("bf16", 8, 7, 10, 65536),      # 488 rows of 64 segments
+    ("bf16", 15, 2, 32, 65536),     # k = 32
+    ("f32", 8, 7, 10, 32768),
+    ("bf16", 8, 7, 10, 65544),      # 65 segments, the last of one vector
 ]
 
 

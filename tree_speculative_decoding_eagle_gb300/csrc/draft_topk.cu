@@ -9,9 +9,10 @@
 // parts of a row form one thread-block cluster.  Few rows (each part fits
 // one segment per warp, and the parts of all rows fit three waves of two
 // CTAs per SM) take 16-warp CTAs with 1024-token segments, held in
-// registers (all 16-byte
-// loads in flight at once); many rows take 8-warp CTAs, three per SM, whose
-// warps stream 1024-token segments through a three-stage ring in shared
+// registers (all 16-byte loads in flight at once); many rows take 8-warp
+// CTAs, three per SM (or 4-warp CTAs, six per SM, when a warp would
+// otherwise see fewer than eight segments), whose warps stream 1024-token
+// segments through a three-stage ring in shared
 // memory (asynchronous copies issued two segments ahead, so the loads stay
 // in flight while a segment is being processed).  A warp visits each
 // segment twice: lane maxima, then the sum of exp(x - segment max), folded
@@ -136,7 +137,8 @@ __device__ __forceinline__ float segment_exp_sum(const uint4 (&vb)[NVL], int nve
 
 // NW warps per CTA, NVL 16-byte vectors per lane and segment.
 template <typename T, int NW, int NVL>
-__global__ void __launch_bounds__(NW * 32, NW <= 8 ? 3 : 2) draft_topk_kernel(DraftArgs a) {
+__global__ void __launch_bounds__(NW * 32, NW == 4 ? 6 : (NW == 8 ? 3 : 2)) draft_topk_kernel(DraftArgs a) {
+  static_assert(NW == 4 || NW == 8 || NW == 16, "4- or 8-warp ring CTAs, 16-warp one-segment CTAs");
   using VT = VecTraits<T>;
   constexpr int VEC = VT::kElems;
   constexpr int SEG = 32 * NVL * VEC;  // tokens per warp and segment
@@ -174,10 +176,10 @@ __global__ void __launch_bounds__(NW * 32, NW <= 8 ? 3 : 2) draft_topk_kernel(Dr
   const int spp = (nseg + a.S - 1) / a.S;
   const int g0 = part * spp, g1 = min(nseg, g0 + spp);
   uint4 vb[NVL];
-  // ring form (8-warp CTAs): warp w's stages at s_ring[(w * kStages + s) *
-  // NVL * 32], lane l's vectors l, l+32, ... of a segment in each; every
-  // iteration commits one copy group (empty past the part's end)
-  constexpr bool kRing = NW == 8;
+  // ring form (4- or 8-warp CTAs): warp w's stages at s_ring[(w * kStages +
+  // s) * NVL * 32], lane l's vectors l, l+32, ... of a segment in each;
+  // every iteration commits one copy group (empty past the part's end)
+  constexpr bool kRing = NW <= 8;
   constexpr int kStages = 3;
   extern __shared__ __align__(16) uint4 s_ring[];
   uint4 *my_ring = s_ring + warp * kStages * NVL * 32;
@@ -416,18 +418,20 @@ __global__ void __launch_bounds__(NW * 32, NW <= 8 ? 3 : 2) draft_topk_kernel(Dr
       // element of this part (or -inf), whenever it is read, and distinct
       // slots hold distinct elements, so the k-th largest of any slots
       // bounds the part's k-th largest from below.  Every eighth segment a
-      // warp takes the maxima of 32 groups of 8 slots and raises the shared
-      // bound to their k-th largest.
+      // warp takes the maxima of 32 groups of NW slots (lane l: slots
+      // NW*l .. NW*l+NW-1 of the NW*32) and raises the shared bound to their
+      // k-th largest.
       s_lmax[tid] = lmax;
       if (((it + warp) & 7) == 0) {
-        float g[8];
-        asm volatile("ld.volatile.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                     : "=f"(g[0]), "=f"(g[1]), "=f"(g[2]), "=f"(g[3]) : "r"(smem_u32(s_lmax + 8 * lane)));
-        asm volatile("ld.volatile.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                     : "=f"(g[4]), "=f"(g[5]), "=f"(g[6]), "=f"(g[7]) : "r"(smem_u32(s_lmax + 8 * lane + 4)));
+        float g[NW];
+#pragma unroll
+        for (int h = 0; h < NW; h += 4)
+          asm volatile("ld.volatile.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                       : "=f"(g[h]), "=f"(g[h + 1]), "=f"(g[h + 2]), "=f"(g[h + 3])
+                       : "r"(smem_u32(s_lmax + NW * lane + h)));
         float gm = g[0];
 #pragma unroll
-        for (int e = 1; e < 8; ++e) gm = fmaxf(gm, g[e]);
+        for (int e = 1; e < NW; ++e) gm = fmaxf(gm, g[e]);
         const float y = warp_sort_desc(gm, lane);
         const float kth = __shfl_sync(0xffffffffu, y, k - 1);
         if (kth > thr) {
@@ -674,8 +678,9 @@ struct DraftPlan {
 // be split into parts of one segment per warp and the parts take at most
 // three waves of two CTAs per SM.  Otherwise 8-warp CTAs streaming 1024-token
 // segments through a shared-memory ring: enough parts for about three CTAs
-// per SM, but no part smaller than one segment per warp.  At most
-// kMaxDraftParts parts per row (one cluster).
+// per SM, but no part smaller than one segment per warp; or, when that
+// leaves a warp fewer than eight segments, 4-warp CTAs (six per SM).  At
+// most kMaxDraftParts parts per row (one cluster).
 static DraftPlan draft_plan(int B, int R, int V, int vec, int num_sms) {
   const int64_t rows = static_cast<int64_t>(B) * R;
   DraftPlan p;
@@ -700,6 +705,18 @@ static DraftPlan draft_plan(int B, int R, int V, int vec, int num_sms) {
   p.NW = 8;
   p.NVL = 4;
   p.S = static_cast<int>(S);
+  // Fewer than eight segments per warp leave the ring's fill and the block
+  // merge unamortised: 4-warp CTAs instead, six per SM, with parts of at
+  // least eight segments per warp where the row has them.
+  if ((nseg + S * 8 - 1) / (S * 8) < 8) {
+    int64_t S4 = (static_cast<int64_t>(num_sms) * 6 + rows - 1) / rows;
+    const int64_t max4 = nseg / 32 > 1 ? nseg / 32 : 1;
+    if (S4 > max4) S4 = max4;
+    if (S4 > kMaxDraftParts) S4 = kMaxDraftParts;
+    if (S4 < 1) S4 = 1;
+    p.NW = 4;
+    p.S = static_cast<int>(S4);
+  }
   return p;
 }
 
@@ -707,18 +724,24 @@ static DraftPlan draft_plan(int B, int R, int V, int vec, int num_sms) {
 // workspace.
 size_t draft_workspace_bytes(int, int, int, int, int, int) { return 0; }
 
-// 8-warp CTAs: three ring stages of 4 vectors per lane for each warp
-constexpr int kRingBytes = 8 * 3 * 4 * 32 * 16;
+// Ring CTAs of NW warps: three stages of 4 vectors per lane for each warp.
+constexpr int ring_bytes(int nw) { return nw * 3 * 4 * 32 * 16; }
+
+template <typename T, int NW>
+static cudaError_t launch_ring(const DraftArgs &a, const dim3 &grid, cudaStream_t st) {
+  static std::atomic<unsigned long long> configured{0};
+  const cudaError_t e = set_smem_limit_once(draft_topk_kernel<T, NW, 4>, ring_bytes(NW), configured);
+  if (e != cudaSuccess) return e;
+  return launch_chained_cluster(draft_topk_kernel<T, NW, 4>, grid, dim3(NW * 32), ring_bytes(NW), st, a.S, a);
+}
 
 template <typename T>
 static cudaError_t launch_t(const DraftArgs &a, const DraftPlan &p, cudaStream_t st) {
   const dim3 grid(a.S, a.B * a.R);
   if (p.NW == 16)
     return launch_chained_cluster(draft_topk_kernel<T, 16, 4>, grid, dim3(16 * 32), 0, st, a.S, a);
-  static std::atomic<unsigned long long> configured{0};
-  const cudaError_t e = set_smem_limit_once(draft_topk_kernel<T, 8, 4>, kRingBytes, configured);
-  if (e != cudaSuccess) return e;
-  return launch_chained_cluster(draft_topk_kernel<T, 8, 4>, grid, dim3(8 * 32), kRingBytes, st, a.S, a);
+  if (p.NW == 4) return launch_ring<T, 4>(a, grid, st);
+  return launch_ring<T, 8>(a, grid, st);
 }
 
 cudaError_t launch_draft_topk(const void *logits, int dtype, int B, int D, int k, int V,
