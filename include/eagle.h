@@ -545,7 +545,8 @@ int eagle_step(const eagle_step_args *args, void *workspace,
  * outputs are then those of that run), then records the step on that
  * stream (capture mode local to the calling thread) and instantiates the
  * graph.  Unlike the other calls it allocates (the stream and the graph)
- * and synchronises; the launches do neither.  On failure *graph is NULL. */
+ * and synchronises; the launches do neither.  On failure *graph is NULL.
+ * Destroy a graph only after the launches made with it have completed. */
 typedef struct eagle_step_graph_s *eagle_step_graph_t;
 
 int eagle_step_graph_create(const eagle_step_args *args, void *workspace,

@@ -444,6 +444,8 @@ class StepGraph:
         _check(load_library().eagle_step_graph_launch(self._h, _stream(stream)), "eagle_step_graph_launch")
 
     def close(self):
+        """Destroys the graph; its launches must have completed (synchronise
+        the streams they were issued on first)."""
         if self._h is not None:
             _check(load_library().eagle_step_graph_destroy(self._h), "eagle_step_graph_destroy")
             self._h = None
